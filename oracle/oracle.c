@@ -1,0 +1,390 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for RMSNorm (forward, residual-fused
+ * forward, backward).  TEST INFRASTRUCTURE: only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg load this file.  It shares no
+ * code, header, table or helper with the CUDA library and never touches a GPU.
+ *
+ * What it computes follows "Skill: Write a Triton RMSNorm Kernel" (ahel.ai,
+ * write-triton-rmsnorm-kernel):
+ *   - Purpose:                 y = x * rsqrt(mean(x^2 over the last axis) + eps) * weight
+ *   - Required reasoning 5-8:  mean of squares over the full row length H,
+ *                              eps inside the square root, weight indexed by
+ *                              column only, apply order (x * rrms) * w
+ *   - Kernel design rules:     fused residual: add the two inputs before squaring
+ *   - Required reasoning 10:   the saved per-row statistic is rrms (reciprocal)
+ *   - Required reasoning 12:   dx = rrms*(dy*w) - (xhat*rrms/H) * sum_h(dy*w*xhat),
+ *                              xhat = x*rrms;  dweight = sum over rows of dy*xhat
+ * and the PyTorch one-liner printed on the "Rocm Kernels" page
+ * (skillselion.com huggingface/kernels/rocm-kernels, "Compare with PyTorch
+ * reference"), which states the same forward.
+ *
+ * Everything is evaluated in IEEE binary64, in plain ascending index order,
+ * with no blocking or reordering.  Storage formats are decoded to binary64 on
+ * entry and results are returned in binary64; rounding back to a storage
+ * format is a separate call (orc_encode), written from the IEEE 754 format
+ * definitions (binary16, and bfloat16 = the upper 16 bits of binary32).
+ *
+ * Threads: rows are independent, so row loops are split into contiguous row
+ * ranges, one per thread.  Each row is computed exactly as in the
+ * single-thread case, so results do not depend on the thread count.  The
+ * cross-row dweight sum is split by column ranges; every column is summed
+ * over rows in ascending row order.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_F64 = 3 };
+
+#define ORC_MAX_THREADS 256
+
+/* ------------------------------------------------------------------------ */
+/* Storage-format codec (IEEE 754-2008 binary16; bfloat16 = binary32's top  */
+/* half; binary32 and binary64 as the C types).                             */
+/* ------------------------------------------------------------------------ */
+
+static double decode_f16(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 10) & 0x1f;
+    int m = b & 0x3ff;
+    double v;
+    if (e == 0)              /* zero or subnormal: m * 2^-24 */
+        v = ldexp((double)m, -24);
+    else if (e == 31)        /* infinity or NaN */
+        v = (m == 0) ? INFINITY : NAN;
+    else                     /* normal: (1024 + m) * 2^(e - 15 - 10) */
+        v = ldexp((double)(1024 + m), e - 25);
+    return sign ? -v : v;
+}
+
+static double decode_bf16(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int m = b & 0x7f;
+    double v;
+    if (e == 0)              /* zero or subnormal: m * 2^-133 */
+        v = ldexp((double)m, -133);
+    else if (e == 255)
+        v = (m == 0) ? INFINITY : NAN;
+    else                     /* normal: (128 + m) * 2^(e - 127 - 7) */
+        v = ldexp((double)(128 + m), e - 134);
+    return sign ? -v : v;
+}
+
+/*
+ * Round |v| to a binary format with `p` significand bits (including the
+ * implicit one), minimum normal exponent `emin`, maximum exponent `emax`,
+ * round-to-nearest, ties to even.  Returns the encoded magnitude bits
+ * (exponent field << (p-1) | fraction) or -1 for overflow to infinity.
+ * Scaling by powers of two is exact in binary64 for every value used here,
+ * so the only rounding step is rint() in the default (nearest-even) mode.
+ */
+static long round_to_format(double a, int p, int emin, int emax, int bias)
+{
+    if (a == 0.0)
+        return 0;
+    int e2;
+    frexp(a, &e2);           /* a = f * 2^e2, f in [0.5, 1) */
+    int e = e2 - 1;          /* a in [2^e, 2^(e+1)) */
+    if (e < emin) {
+        /* subnormal range: integer multiple of 2^(emin - p + 1) */
+        double q = rint(ldexp(a, -(emin - p + 1)));
+        /* q may reach 2^(p-1): that is the smallest normal, whose encoding
+           (exponent field 1, fraction 0) equals q as an integer. */
+        return (long)q;
+    }
+    double q = rint(ldexp(a, (p - 1) - e));    /* in [2^(p-1), 2^p] */
+    if (q == ldexp(1.0, p)) {                  /* rounded up to the next binade */
+        q = ldexp(1.0, p - 1);
+        e += 1;
+    }
+    if (e > emax)
+        return -1;
+    return ((long)(e + bias) << (p - 1)) | ((long)q - (1L << (p - 1)));
+}
+
+static uint16_t encode_f16(double v)
+{
+    if (isnan(v))
+        return 0x7e00;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    long mag = round_to_format(fabs(v), 11, -14, 15, 15);
+    if (mag < 0 || isinf(v))
+        return sign | 0x7c00;
+    return sign | (uint16_t)mag;
+}
+
+static uint16_t encode_bf16(double v)
+{
+    if (isnan(v))
+        return 0x7fc0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    long mag = round_to_format(fabs(v), 8, -126, 127, 127);
+    if (mag < 0 || isinf(v))
+        return sign | 0x7f80;
+    return sign | (uint16_t)mag;
+}
+
+static size_t elem_size(int dtype)
+{
+    switch (dtype) {
+    case ORC_F32: return 4;
+    case ORC_F16: return 2;
+    case ORC_BF16: return 2;
+    case ORC_F64: return 8;
+    default: return 0;
+    }
+}
+
+/* element k of a storage array, as binary64 */
+static double load_elem(int dtype, const void *base, int64_t k)
+{
+    switch (dtype) {
+    case ORC_F32: return (double)((const float *)base)[k];
+    case ORC_F16: return decode_f16(((const uint16_t *)base)[k]);
+    case ORC_BF16: return decode_bf16(((const uint16_t *)base)[k]);
+    default: return ((const double *)base)[k];
+    }
+}
+
+int orc_decode(int dtype, const void *src, double *dst, int64_t n)
+{
+    if (!elem_size(dtype))
+        return 1;
+    for (int64_t k = 0; k < n; ++k)
+        dst[k] = load_elem(dtype, src, k);
+    return 0;
+}
+
+/* binary64 -> storage format, each value rounded once (nearest, ties even) */
+int orc_encode(int dtype, const double *src, void *dst, int64_t n)
+{
+    for (int64_t k = 0; k < n; ++k) {
+        switch (dtype) {
+        case ORC_F32: ((float *)dst)[k] = (float)src[k]; break;
+        case ORC_F16: ((uint16_t *)dst)[k] = encode_f16(src[k]); break;
+        case ORC_BF16: ((uint16_t *)dst)[k] = encode_bf16(src[k]); break;
+        case ORC_F64: ((double *)dst)[k] = src[k]; break;
+        default: return 1;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Row-parallel driver                                                      */
+/* ------------------------------------------------------------------------ */
+
+typedef void (*range_fn)(void *ctx, int64_t begin, int64_t end);
+
+struct range_job {
+    range_fn fn;
+    void *ctx;
+    int64_t begin, end;
+};
+
+static void *range_thread(void *p)
+{
+    struct range_job *j = (struct range_job *)p;
+    j->fn(j->ctx, j->begin, j->end);
+    return NULL;
+}
+
+/* run fn over [0, n) split into at most nthreads contiguous ranges */
+static void parallel_ranges(range_fn fn, void *ctx, int64_t n, int nthreads)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > ORC_MAX_THREADS)
+        nthreads = ORC_MAX_THREADS;
+    if ((int64_t)nthreads > n)
+        nthreads = (int)(n > 0 ? n : 1);
+    if (nthreads == 1) {
+        fn(ctx, 0, n);
+        return;
+    }
+    pthread_t tid[ORC_MAX_THREADS];
+    struct range_job job[ORC_MAX_THREADS];
+    int started[ORC_MAX_THREADS];
+    for (int t = 0; t < nthreads; ++t) {
+        job[t].fn = fn;
+        job[t].ctx = ctx;
+        job[t].begin = n * t / nthreads;
+        job[t].end = n * (t + 1) / nthreads;
+        started[t] = pthread_create(&tid[t], NULL, range_thread, &job[t]) == 0;
+        if (!started[t])
+            fn(ctx, job[t].begin, job[t].end);   /* no thread: run it here */
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (started[t])
+            pthread_join(tid[t], NULL);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Forward                                                                  */
+/* ------------------------------------------------------------------------ */
+
+struct fwd_ctx {
+    int dtype;
+    const void *x, *r, *w;
+    int64_t H, stride;
+    double eps;
+    double *y, *s_out, *rrms;
+};
+
+static void fwd_rows(void *p, int64_t i0, int64_t i1)
+{
+    const struct fwd_ctx *c = (const struct fwd_ctx *)p;
+    const int64_t H = c->H;
+    double *s = (double *)malloc((size_t)H * sizeof(double));
+    if (!s)
+        abort();
+    for (int64_t i = i0; i < i1; ++i) {
+        const int64_t row = i * c->stride;
+        /* input row; fused residual: s = x + r, added before squaring */
+        for (int64_t h = 0; h < H; ++h) {
+            s[h] = load_elem(c->dtype, c->x, row + h);
+            if (c->r)
+                s[h] += load_elem(c->dtype, c->r, row + h);
+        }
+        /* mean of squares over the full row length H */
+        double ss = 0.0;
+        for (int64_t h = 0; h < H; ++h)
+            ss += s[h] * s[h];
+        const double ms = ss / (double)H;
+        /* reciprocal RMS, eps inside the square root */
+        const double rrms = 1.0 / sqrt(ms + c->eps);
+        if (c->rrms)
+            c->rrms[i] = rrms;
+        /* y = (s * rrms) * w, weight indexed by column only */
+        for (int64_t h = 0; h < H; ++h) {
+            double w = c->w ? load_elem(c->dtype, c->w, h) : 1.0;
+            c->y[i * H + h] = (s[h] * rrms) * w;
+            if (c->s_out)
+                c->s_out[i * H + h] = s[h];
+        }
+    }
+    free(s);
+}
+
+/*
+ * x, r (nullable: no residual), w (nullable: no weight) are storage arrays;
+ * element (i, h) of x and r sits at index i*stride + h, element h of w at h.
+ * eps is the binary64 value of the binary32 eps the library receives.
+ * Outputs are dense M x H binary64 (y, s_out) and M binary64 (rrms);
+ * s_out and rrms are nullable.
+ */
+int orc_rmsnorm_fwd(int dtype, const void *x, const void *r, const void *w,
+                    int64_t M, int64_t H, int64_t stride, double eps,
+                    double *y, double *s_out, double *rrms, int nthreads)
+{
+    if (!elem_size(dtype) || !x || !y || M < 0 || H <= 0 || stride < H)
+        return 1;
+    struct fwd_ctx c = {dtype, x, r, w, H, stride, eps, y, s_out, rrms};
+    parallel_ranges(fwd_rows, &c, M, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward                                                                 */
+/* ------------------------------------------------------------------------ */
+
+struct bwd_ctx {
+    int dtype;
+    const void *dy, *x, *w;
+    int64_t M, H, stride;
+    double eps;
+    double *dx, *dweight, *dweight_abs, *rrms;
+};
+
+/* rrms per row, recomputed in binary64 from the stored input row */
+static void bwd_rrms_rows(void *p, int64_t i0, int64_t i1)
+{
+    const struct bwd_ctx *c = (const struct bwd_ctx *)p;
+    for (int64_t i = i0; i < i1; ++i) {
+        double ss = 0.0;
+        for (int64_t h = 0; h < c->H; ++h) {
+            double v = load_elem(c->dtype, c->x, i * c->stride + h);
+            ss += v * v;
+        }
+        c->rrms[i] = 1.0 / sqrt(ss / (double)c->H + c->eps);
+    }
+}
+
+/* dx_h = rrms*g_h - xhat_h*(rrms/H)*sum_k g_k*xhat_k, g = dy*w, xhat = x*rrms */
+static void bwd_dx_rows(void *p, int64_t i0, int64_t i1)
+{
+    const struct bwd_ctx *c = (const struct bwd_ctx *)p;
+    const int64_t H = c->H;
+    for (int64_t i = i0; i < i1; ++i) {
+        const int64_t row = i * c->stride;
+        const double rrms = c->rrms[i];
+        double dot = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            double w = c->w ? load_elem(c->dtype, c->w, h) : 1.0;
+            double g = load_elem(c->dtype, c->dy, row + h) * w;
+            double xhat = load_elem(c->dtype, c->x, row + h) * rrms;
+            dot += g * xhat;
+        }
+        for (int64_t h = 0; h < H; ++h) {
+            double w = c->w ? load_elem(c->dtype, c->w, h) : 1.0;
+            double g = load_elem(c->dtype, c->dy, row + h) * w;
+            double xhat = load_elem(c->dtype, c->x, row + h) * rrms;
+            c->dx[i * H + h] = rrms * g - xhat * (rrms / (double)H) * dot;
+        }
+    }
+}
+
+/* dweight_h = sum over rows i (ascending) of dy_ih * xhat_ih; also the sum of
+   absolute terms, which bounds the rounding error of any summation order */
+static void bwd_dweight_cols(void *p, int64_t h0, int64_t h1)
+{
+    const struct bwd_ctx *c = (const struct bwd_ctx *)p;
+    for (int64_t h = h0; h < h1; ++h) {
+        double acc = 0.0, acc_abs = 0.0;
+        for (int64_t i = 0; i < c->M; ++i) {
+            double t = load_elem(c->dtype, c->dy, i * c->stride + h) *
+                       (load_elem(c->dtype, c->x, i * c->stride + h) * c->rrms[i]);
+            acc += t;
+            acc_abs += fabs(t);
+        }
+        if (c->dweight)
+            c->dweight[h] = acc;
+        if (c->dweight_abs)
+            c->dweight_abs[h] = acc_abs;
+    }
+}
+
+/*
+ * dy, x storage arrays with row stride `stride`; w nullable (no weight: g = dy).
+ * Outputs (all nullable): dx dense M x H binary64, dweight and dweight_abs H
+ * binary64, rrms M binary64 (recomputed from x; scratch is allocated here if
+ * the caller passes NULL).
+ */
+int orc_rmsnorm_bwd(int dtype, const void *dy, const void *x, const void *w,
+                    int64_t M, int64_t H, int64_t stride, double eps,
+                    double *dx, double *dweight, double *dweight_abs, double *rrms,
+                    int nthreads)
+{
+    if (!elem_size(dtype) || !dy || !x || M < 0 || H <= 0 || stride < H)
+        return 1;
+    double *rr = rrms;
+    if (!rr) {
+        rr = (double *)malloc((size_t)(M > 0 ? M : 1) * sizeof(double));
+        if (!rr)
+            return 2;
+    }
+    struct bwd_ctx c = {dtype, dy, x, w, M, H, stride, eps, dx, dweight, dweight_abs, rr};
+    parallel_ranges(bwd_rrms_rows, &c, M, nthreads);
+    if (dx)
+        parallel_ranges(bwd_dx_rows, &c, M, nthreads);
+    if (dweight || dweight_abs)
+        parallel_ranges(bwd_dweight_cols, &c, H, nthreads);
+    if (!rrms)
+        free(rr);
+    return 0;
+}
