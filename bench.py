@@ -1,0 +1,491 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 RMSNorm engine.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                    [--workload step|fwd_f32|fused_fwd|dit_mix|fwd_bwd_8192|fused_f16_padded]
+
+Default workload ("step"): one pass of the whole hot path on the
+(B=8, T=2048, H=4096) bf16 activations, M = 16384 rows -- the fused
+residual-add + RMSNorm forward (x, residual -> y, residual_out, rrms) followed
+by the backward on its output (dy, residual_out, rrms -> dx, dweight).  Inputs
+are seeded synthetic N(0, 1) activations and a 1 + 0.1 N(0, 1) weight.
+The metric is achieved HBM bandwidth over the algorithmic bytes (every M x H
+tensor read or written once, plus weight, rrms and dweight), with rows/s
+beside it.
+
+Prints ONE JSON line (rank 0).  Timing: W untimed warm-up steps, then K
+steps between a barrier + synchronize on both sides, CUDA events on the
+launching stream, max over ranks.  The per-step working set (~0.94 GB) is
+larger than L2, so no flush is needed between steps.
+
+``--impl reference`` times the fp64 CPU oracle (the only other implementation
+of this method here) on a bounded row sample of the same workload, on the
+host cores, and prints the same line shape with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and rows/s for residual+RMSNorm fwd/bwd"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["residual_add_rmsnorm_fwd_gb300/csrc/*.cu", "residual_add_rmsnorm_fwd_gb300/csrc/*.cuh",
+                  "residual_add_rmsnorm_fwd_gb300/csrc/*.h"]
+
+
+# --------------------------------------------------------------------------
+# small host utilities (no GPU needed; unit-tested on CPU)
+# --------------------------------------------------------------------------
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for pat in KERNEL_SOURCES:
+        for p in sorted(glob.glob(os.path.join(ROOT, pat))):
+            h.update(os.path.basename(p).encode())
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    """(GB/s, source) from the generated peaks file, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel_label: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/, or
+    None when no summary exists or the kernels changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_label}.md")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                rec[k.strip()] = v.strip().strip("`")
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def aggregate(per_rank_ms, units_per_rank, bytes_per_unit_rank):
+    """Whole-job numbers from per-rank timings: every rank processed the same
+    units; the job time is the slowest rank's."""
+    t = max(per_rank_ms)
+    n = len(per_rank_ms)
+    return {"ms": t, "units_per_s": n * units_per_rank / (t / 1e3),
+            "gbs": n * bytes_per_unit_rank / (t / 1e3) / 1e9}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu, self.period, self.proc, self.out = gpu_index, period_ms, None, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period), "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return parse_clock_lines(out.splitlines())
+
+
+def parse_clock_lines(lines):
+    rows = []
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) != len(ClockSampler.FIELDS):
+            continue
+        try:
+            ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            rows.append({"t": ts + frac, "sm": float(parts[2]), "sm_max": float(parts[3]),
+                         "power": float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else None,
+                         "hw_slowdown": parts[6] == "Active", "hw_thermal_slowdown": parts[7] == "Active",
+                         "sw_thermal_slowdown": parts[8] == "Active", "sw_power_cap": parts[9] == "Active"})
+        except (ValueError, IndexError):
+            continue
+    return rows
+
+
+def summarize_clocks(rows, t0, t1):
+    inside = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05]
+    use = inside if inside else rows
+    if not use:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    reasons = sorted({k for r in use for k in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                                "sw_power_cap") if r[k]})
+    return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["sm_max"] for r in use),
+            "reasons": reasons, "samples": len(use), "in_window": bool(inside)}
+
+
+# --------------------------------------------------------------------------
+# workloads
+# --------------------------------------------------------------------------
+
+def step_bytes(M, H, es, fused=True, weight=True, save_rrms=True, backward=True):
+    """Algorithmic bytes: each M x H tensor once, plus weight, rrms, dweight."""
+    mh = M * H * es
+    fwd = (4 if fused else 2) * mh + (H * es if weight else 0) + (M * 4 if save_rrms else 0)
+    bwd = (3 * mh + M * 4 + (H * es + H * 4 if weight else 0)) if backward else 0
+    return fwd, bwd
+
+
+class StepWorkload:
+    """Fused forward + backward on one batch (the default benchmark step)."""
+    name = "fused_fwd_bwd_bf16_B8xT2048xH4096"
+
+    def __init__(self, cfg_id=2, backward=True, fused=None):
+        import torch
+        import residual_add_rmsnorm_fwd_gb300 as rn
+        import workloads as wl
+        self.torch, self.rn, self.wl = torch, rn, wl
+        c = wl.CONFIGS[cfg_id]
+        self.c, self.cfg_id = c, cfg_id
+        self.fused = c["residual"] if fused is None else fused
+        self.backward = backward
+        self.M, self.H, self.S, self.dt = c["M"], c["H"], c["stride"], c["dtype"]
+        self.es = wl.ELEM_BYTES[self.dt]
+        self.fwd_bytes, self.bwd_bytes = step_bytes(self.M, self.H, self.es, self.fused, True, backward, backward)
+        self.bytes_per_step = self.fwd_bytes + self.bwd_bytes
+        self.rows_per_step = self.M
+        self.host = wl.generate(cfg_id, with_dy=backward)
+        self.kernels_per_step = 1 + (2 if backward else 0)
+
+    def setup(self):
+        torch, wl, dt = self.torch, self.wl, self.dt
+        tdt = wl.torch_dtype(dt)
+        dev = torch.device("cuda")
+
+        def up(a):
+            return wl.to_torch(a, dt).to(dev)
+
+        M, H, S = self.M, self.H, self.S
+        self.x = up(self.host["x"])[:, :H]
+        self.r = up(self.host["residual"])[:, :H] if self.fused else None
+        self.w = up(self.host["w"])
+        self.y = torch.empty(M, S, dtype=tdt, device=dev)[:, :H]
+        self.s = torch.empty(M, S, dtype=tdt, device=dev)[:, :H] if self.fused else None
+        self.rrms = torch.empty(M, device=dev) if self.backward else None
+        if self.backward:
+            self.dy = up(self.host["dy"])[:, :H]
+            self.dx = torch.empty(M, S, dtype=tdt, device=dev)[:, :H]
+            self.dw = torch.empty(H, device=dev)
+            self.ws = torch.empty(max(1, self.rn.rmsnorm_bwd_workspace_bytes(M, H, tdt)), dtype=torch.uint8,
+                                  device=dev)
+        return self
+
+    def calls(self):
+        """[(label, fn, algorithmic bytes)] enqueued on the current stream, in order."""
+        rn, eps = self.rn, self.c["eps"]
+        out = []
+        if self.fused:
+            out.append(("fwd_residual", lambda: rn.rmsnorm_fwd_residual(self.x, self.r, self.w, self.y, self.s,
+                                                                        self.rrms, eps=eps), self.fwd_bytes))
+        else:
+            out.append(("fwd", lambda: rn.rmsnorm_fwd(self.x, self.w, self.y, self.rrms, eps=eps), self.fwd_bytes))
+        if self.backward:
+            xin = self.s if self.fused else self.x
+            out.append(("bwd", lambda: rn.rmsnorm_bwd(self.dy, xin, self.w, self.rrms, self.dx, self.dw, self.ws),
+                        self.bwd_bytes))
+        return out
+
+    def config(self):
+        return {"workload": self.name, "M": self.M, "H": self.H, "row_stride": self.S, "dtype": self.dt,
+                "B": 8, "T": 2048, "fused_residual": self.fused, "backward": self.backward,
+                "eps": self.c["eps"], "l2": "no flush: per-step working set larger than L2",
+                "algorithmic_bytes_per_step": self.bytes_per_step}
+
+    # end to end through the binding with pinned host buffers
+    def e2e_setup(self):
+        torch = self.torch
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
+        self.hx = self.wl.to_torch(self.host["x"], self.dt)[:, :self.H].contiguous().pin_memory()
+        self.hr = (self.wl.to_torch(self.host["residual"], self.dt)[:, :self.H].contiguous().pin_memory()
+                   if self.fused else None)
+        self.hdy = (self.wl.to_torch(self.host["dy"], self.dt)[:, :self.H].contiguous().pin_memory()
+                    if self.backward else None)
+        self.hy = pin(self.y)
+        self.hs = pin(self.s) if self.fused else None
+        self.hdx = pin(self.dx) if self.backward else None
+        self.hdw = pin(self.dw) if self.backward else None
+        ins = [t for t in (self.hx, self.hr, self.hdy) if t is not None]
+        outs = [t for t in (self.hy, self.hs, self.hdx, self.hdw) if t is not None]
+        self.h2d = sum(t.numel() * t.element_size() for t in ins)
+        self.d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def e2e_step(self):
+        self.x.copy_(self.hx, non_blocking=True)
+        if self.fused:
+            self.r.copy_(self.hr, non_blocking=True)
+        if self.backward:
+            self.dy.copy_(self.hdy, non_blocking=True)
+        for _, fn, _ in self.calls():
+            fn()
+        self.hy.copy_(self.y, non_blocking=True)
+        if self.fused:
+            self.hs.copy_(self.s, non_blocking=True)
+        if self.backward:
+            self.hdx.copy_(self.dx, non_blocking=True)
+            self.hdw.copy_(self.dw, non_blocking=True)
+
+    # CPU oracle on a row sample of the same inputs
+    def oracle_step(self, rows):
+        import oracle
+        H, dt, eps = self.H, self.dt, self.c["eps"]
+        x = self.host["x"][:rows, :H]
+        r = self.host["residual"][:rows, :H] if self.fused else None
+        f = oracle.rmsnorm_fwd(x, self.host["w"], eps, dt, residual=r)
+        if self.backward:
+            s = oracle.encode(f["s"], dt)
+            oracle.rmsnorm_bwd(self.host["dy"][:rows, :H], s, self.host["w"], eps, dt)
+        return rows * self.bytes_per_step / self.M
+
+
+WORKLOADS = {
+    "step": lambda: StepWorkload(2, backward=True),
+    "fused_fwd": lambda: StepWorkload(2, backward=False),
+    "fwd_bwd_8192": lambda: StepWorkload(4, backward=True),
+    "fused_f16_padded": lambda: StepWorkload(5, backward=True),
+}
+
+
+# --------------------------------------------------------------------------
+# timing
+# --------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return [v]
+    import torch
+    import torch.distributed as dist
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    out = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(out, t)
+    return [float(o.item()) for o in out]
+
+
+def run_native(args):
+    import torch
+    rank, world, local = dist_setup(args.gpus)
+    wk = WORKLOADS[args.workload]().setup()
+    calls = wk.calls()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        for _, fn, _ in calls:
+            fn()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+          for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local).start() if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for k in range(K):
+        for j, (_, fn, _) in enumerate(calls):
+            ev[k][j][0].record(stream)
+            fn()
+            ev[k][j][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    ms_total = start.elapsed_time(stop)
+    per_call_ms = [[ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(K)] for j in range(len(calls))]
+
+    # end to end with pinned host buffers (fewer steps: host copies dominate)
+    wk.e2e_setup()
+    Ke = max(3, min(K, 20))
+    for _ in range(2):
+        wk.e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        wk.e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = e0.elapsed_time(e1) / Ke
+
+    clocks = summarize_clocks(sampler.stop(), t0, t1) if sampler else None
+    all_ms = max_over_ranks(ms_total / K, world)
+    all_e2e = max_over_ranks(e2e_ms, world)
+    if rank != 0:
+        return None
+
+    agg = aggregate(all_ms, wk.rows_per_step, wk.bytes_per_step)
+    agg_e2e = aggregate(all_e2e, wk.rows_per_step, wk.bytes_per_step)
+    peak, peak_src = measured_peak()
+    kern = {}
+    for j, (label, _, nbytes) in enumerate(calls):
+        avg = sum(per_call_ms[j]) / K
+        kern[label] = {"avg_us": avg * 1e3, "median_us": statistics.median(per_call_ms[j]) * 1e3,
+                       "gbs": nbytes / (avg / 1e3) / 1e9, "algorithmic_bytes": nbytes,
+                       "frac_of_measured_peak": nbytes / (avg / 1e3) / 1e9 / peak,
+                       "share_of_step": sum(per_call_ms[j]) / ms_total}
+    dom = max(kern, key=lambda k: kern[k]["avg_us"])
+    traffic = profile_traffic(f"{dom}_{wk.dt}_{wk.M}x{wk.H}")
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(kern[dom]["gbs"], 1), "peak": peak,
+                "unit": "GB/s", "frac": round(kern[dom]["gbs"] / peak, 4), "peak_source": peak_src,
+                "traffic": traffic, "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
+    line = {
+        "metric": METRIC, "value": round(agg["gbs"], 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(agg["ms"], 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wk.dt, "data": "synthetic (seeded N(0,1) activations, 1+0.1N(0,1) weight)",
+        "config": wk.config(), "rows_per_s": round(agg["units_per_s"], 1),
+        "pct_of_measured_peak": round(100 * agg["gbs"] / peak, 2),
+        "pct_of_nominal_8tbs": round(100 * agg["gbs"] / NOMINAL_HBM_GBS, 2),
+        "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                    for k, v in kern.items()},
+        "roofline": roofline,
+        "e2e": {"value": round(agg_e2e["gbs"], 2), "unit": "GB/s", "h2d_bytes_per_step": wk.h2d,
+                "d2h_bytes_per_step": wk.d2h, "ms_per_step": round(agg_e2e["ms"], 4), "steps": Ke},
+        "gpu_launches": K * wk.kernels_per_step,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wk, budget_s=args.cpu_seconds)
+    return line
+
+
+def cpu_baseline(wk, budget_s=10.0, rows=None):
+    """The fp64 oracle as it stands, all host cores, on the first `rows` rows
+    of the same seeded inputs, repeated for about `budget_s` seconds."""
+    import oracle
+    rows = rows or min(wk.M, 1024)
+    wk.oracle_step(min(rows, 16))  # build + warm
+    n_bytes, t0, reps = 0.0, time.perf_counter(), 0
+    while True:
+        n_bytes += wk.oracle_step(rows)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(n_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.default_threads(),
+            "kind": "oracle", "rows_per_s": round(reps * rows / dt, 1),
+            "sample": f"first {rows} rows of the same seeded workload, fwd+bwd, repeated {reps}x in {dt:.1f}s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    wk = WORKLOADS[args.workload]()
+    import oracle
+    oracle.build()
+    # size the row sample so the whole run stays within about a minute
+    probe_rows = 64
+    t = time.perf_counter()
+    wk.oracle_step(probe_rows)
+    per_row = (time.perf_counter() - t) / probe_rows
+    total_steps = args.steps + args.warmup
+    rows = int(max(8, min(wk.M, 60.0 / max(total_steps, 1) / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        wk.oracle_step(rows)
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for _ in range(args.steps):
+        nbytes += wk.oracle_step(rows)
+    dt = time.perf_counter() - t0
+    gbs = nbytes / dt / 1e9
+    cores = oracle.default_threads()
+    sample = f"first {rows} of {wk.M} rows per step, fwd+bwd fp64 oracle"
+    return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wk.dt,
+            "data": "synthetic", "config": dict(wk.config(), sample_rows=rows),
+            "rows_per_s": round(rows * args.steps / dt, 1),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        import residual_add_rmsnorm_fwd_gb300 as rn
+        rn.lib()  # fail loudly before any work if the library is missing
+        line = run_native(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,144 @@
+/*
+ * rmsnorm.h -- C ABI of librmsnorm_gb300.so, an RMSNorm engine for GB300
+ * (sm_103a).  All compute runs in the library's own CUDA kernels; the
+ * library allocates no memory and keeps no state besides a per-device cache
+ * of launch limits.
+ *
+ * The operation ("Skill: Write a Triton RMSNorm Kernel", ahel.ai, Purpose):
+ *   y = x * rsqrt(mean(x^2 over the trailing dimension H) + eps) * weight
+ * for each of M rows, with
+ *   - the mean taken over the full row length H and eps inside the square
+ *     root (Required reasoning 5-6; Correctness requirements),
+ *   - a per-feature weight of shape (H,) indexed by column only and no bias
+ *     (Required reasoning 7; Kernel design rules),
+ *   - apply order y = (x_f32 * rrms) * w_f32 with one final rounding to the
+ *     storage type (Required reasoning 8),
+ *   - an optional weight: has_weight == 0 gives y = x * rrms, bit-identical
+ *     to a weight of ones (the weightless norm instances of the "Rocm
+ *     Kernels" page, section "Core Kernel Implementations / 1. RMSNorm").
+ *
+ * Common conventions for every entry point:
+ *   - Pointers are device pointers owned by the caller; nothing is retained
+ *     after the call returns.
+ *   - A matrix argument holds M rows of H elements; element (i, h) is at
+ *     index i * row_stride + h (in elements of the storage dtype).  Every
+ *     matrix argument of one call shares row_stride, and row_stride >= H.
+ *     Padding columns h in [H, row_stride) are never read or written.
+ *   - dtype is the storage type of x, residual, weight, y, residual_out, dy
+ *     and dx (rmsn_dtype).  Arithmetic is binary32; every stored result is
+ *     rounded to nearest, ties to even.  rrms and dweight are binary32.
+ *   - Every pointer must be aligned to its element size.  Rows whose byte
+ *     offsets and lengths are multiples of 16 use 128-bit accesses; other
+ *     layouts run a scalar-access variant of the same kernels (on the GPU).
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work and return; errors raised while the kernels run
+ *     surface at the caller's next synchronisation.
+ *   - All arguments are validated before anything is launched.  An invalid
+ *     call returns a nonzero rmsn_status and launches nothing.  M == 0 is a
+ *     valid no-op.
+ *   - An output may not overlap any other argument (byte ranges of the rows
+ *     [0, M) are compared): in-place use is rejected with RMSN_ERR_ALIAS.
+ */
+#ifndef RMSNORM_GB300_H
+#define RMSNORM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RMSN_F32 = 0,
+    RMSN_F16 = 1,  /* IEEE binary16 */
+    RMSN_BF16 = 2  /* bfloat16 */
+} rmsn_dtype;
+
+typedef enum {
+    RMSN_OK = 0,
+    RMSN_ERR_INVALID = 1,     /* NULL required pointer, M < 0, H <= 0, row_stride < H,
+                                 eps < 0 or not finite, unknown dtype, misaligned pointer */
+    RMSN_ERR_ALIAS = 2,       /* an output overlaps another argument */
+    RMSN_ERR_WORKSPACE = 3,   /* backward workspace missing, misaligned or too small */
+    RMSN_ERR_CUDA = 4,        /* a CUDA runtime call or a kernel launch failed */
+    RMSN_ERR_UNSUPPORTED = 5  /* no usable sm_103 device is current */
+} rmsn_status;
+
+/*
+ * Forward.  ("Skill: Write a Triton RMSNorm Kernel": Purpose; Required
+ * reasoning 1-10.)
+ *   x       in   M x H, row_stride
+ *   weight  in   H elements; ignored (may be NULL) when has_weight == 0
+ *   y       out  M x H, row_stride
+ *   rrms    out  M binary32 values 1/sqrt(mean(x^2) + eps), the statistic the
+ *                backward reads (Required reasoning 10); NULL = not saved
+ *   eps     >= 0 and finite.  eps == 0 is accepted: a row of zeros then
+ *           yields NaN.
+ * Returns RMSN_OK or an rmsn_status error code.
+ */
+int rmsnorm_fwd(const void *x, const void *weight, void *y, float *rrms,
+                int64_t row_stride, int64_t M, int64_t H, float eps,
+                int dtype, int has_weight, void *stream);
+
+/*
+ * Forward with the residual add fused in front of the norm.  ("Skill: Write
+ * a Triton RMSNorm Kernel": Use this when, third bullet; Inputs 7; Kernel
+ * design rules, fused residual.)
+ *   s = x + residual is formed in binary32 before squaring;
+ *   residual_out = s rounded to dtype (the next block's residual stream);
+ *   y = norm(s) * weight, normalising the unrounded binary32 s.
+ *   x, residual   in   M x H, row_stride
+ *   weight        in   H elements; ignored when has_weight == 0
+ *   y             out  M x H, row_stride
+ *   residual_out  out  M x H, row_stride
+ *   rrms          out  M binary32 values (NULL = not saved)
+ * The backward of this call is rmsnorm_bwd with x := residual_out; its dx
+ * is the gradient for both x and residual.
+ */
+int rmsnorm_fwd_residual(const void *x, const void *residual, const void *weight,
+                         void *y, void *residual_out, float *rrms,
+                         int64_t row_stride, int64_t M, int64_t H, float eps,
+                         int dtype, int has_weight, void *stream);
+
+/*
+ * Size in bytes of the workspace rmsnorm_bwd needs for (M, H, dtype) on the
+ * current device (per-CTA binary32 dweight partials).  Writes *bytes; the
+ * value is fixed for a given device, M, H and dtype.  0 means no workspace
+ * is needed.
+ */
+int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype, size_t *bytes);
+
+/*
+ * Backward.  ("Skill: Write a Triton RMSNorm Kernel": Required reasoning 12;
+ * Correctness requirements on the saved rrms and the dweight axis.)
+ * With g = dy * w and xhat = x * rrms (w = 1 when has_weight == 0):
+ *   dx_h      = rrms * (g_h - xhat_h * (1/H) * sum_k g_k * xhat_k)
+ *   dweight_h = sum over rows i of dy_ih * xhat_ih
+ *   dy         in   M x H, row_stride
+ *   x          in   M x H, row_stride: the forward's normalised input
+ *                   (residual_out for the residual-fused forward)
+ *   weight     in   H elements; ignored when has_weight == 0
+ *   rrms       in   M binary32 values saved by the forward (not recomputed)
+ *   dx         out  M x H, row_stride
+ *   dweight    out  H binary32 values, or NULL to skip it; ignored when
+ *                   has_weight == 0.  Deterministic: per-CTA partial sums
+ *                   over a fixed row assignment, then a fixed-order column
+ *                   sum, so repeated calls on one device give identical bits.
+ *   workspace  scratch of at least rmsnorm_bwd_workspace_bytes(M, H, dtype)
+ *              bytes, 16-byte aligned; needed only when dweight is computed
+ *              (may be NULL otherwise).  Contents on entry are ignored.
+ */
+int rmsnorm_bwd(const void *dy, const void *x, const void *weight, const float *rrms,
+                void *dx, float *dweight, void *workspace, size_t workspace_bytes,
+                int64_t row_stride, int64_t M, int64_t H,
+                int dtype, int has_weight, void *stream);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char *rmsnorm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_GB300_H */

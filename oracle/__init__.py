@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -32,7 +33,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
-_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_LIB_PATH = os.path.join(_HERE, f"liboracle.{platform.machine()}.so")
 
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "f64": 3}
 STORAGE = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16, "f64": np.float64}
@@ -42,7 +43,7 @@ _lock = threading.Lock()
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so next to it (gcc, -O2, no fast-math)."""
+    """Compile oracle.c into liboracle.<arch>.so next to it (gcc, -O2, no fast-math)."""
     up_to_date = (os.path.exists(_LIB_PATH)
                   and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC))
     if force or not up_to_date:

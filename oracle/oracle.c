@@ -340,23 +340,34 @@ static void bwd_dx_rows(void *p, int64_t i0, int64_t i1)
 }
 
 /* dweight_h = sum over rows i (ascending) of dy_ih * xhat_ih; also the sum of
-   absolute terms, which bounds the rounding error of any summation order */
+   absolute terms, which bounds the rounding error of any summation order.
+   A thread owns a column range and walks the rows in ascending order, so
+   every column is summed in ascending row order. */
 static void bwd_dweight_cols(void *p, int64_t h0, int64_t h1)
 {
     const struct bwd_ctx *c = (const struct bwd_ctx *)p;
-    for (int64_t h = h0; h < h1; ++h) {
-        double acc = 0.0, acc_abs = 0.0;
-        for (int64_t i = 0; i < c->M; ++i) {
-            double t = load_elem(c->dtype, c->dy, i * c->stride + h) *
-                       (load_elem(c->dtype, c->x, i * c->stride + h) * c->rrms[i]);
-            acc += t;
-            acc_abs += fabs(t);
+    const int64_t n = h1 - h0;
+    double *acc = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    double *acc_abs = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    if (!acc || !acc_abs)
+        abort();
+    for (int64_t i = 0; i < c->M; ++i) {
+        const int64_t row = i * c->stride;
+        for (int64_t h = h0; h < h1; ++h) {
+            double t = load_elem(c->dtype, c->dy, row + h) *
+                       (load_elem(c->dtype, c->x, row + h) * c->rrms[i]);
+            acc[h - h0] += t;
+            acc_abs[h - h0] += fabs(t);
         }
-        if (c->dweight)
-            c->dweight[h] = acc;
-        if (c->dweight_abs)
-            c->dweight_abs[h] = acc_abs;
     }
+    for (int64_t h = h0; h < h1; ++h) {
+        if (c->dweight)
+            c->dweight[h] = acc[h - h0];
+        if (c->dweight_abs)
+            c->dweight_abs[h] = acc_abs[h - h0];
+    }
+    free(acc);
+    free(acc_abs);
 }
 
 /*

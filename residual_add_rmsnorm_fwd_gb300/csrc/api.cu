@@ -1,0 +1,282 @@
+// api.cu -- the extern "C" entry points of include/rmsnorm.h: argument
+// validation (all of it before any launch), per-device limits, kernel choice
+// and launch.
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/rmsnorm.h"
+#include "launch.h"
+
+namespace rmsn {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxH = int64_t(1) << 24;   // H is exact in binary32 up to 2^24
+constexpr int kSmallH = 256;                  // warp-per-row kernel below this
+
+struct DevInfo {
+    bool checked = false;
+    int status = RMSN_OK;
+    int sm_count = 0;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+std::map<std::tuple<int, const void *, int, size_t>, int> g_occ;
+
+// Kernel image for sm_103 only: check the current device once.
+int current_device(int *dev_out, int *sm_count) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RMSN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.checked) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            return RMSN_ERR_CUDA;
+        }
+        d.status = (major == 10 && minor == 3 && sms > 0) ? RMSN_OK : RMSN_ERR_UNSUPPORTED;
+        d.sm_count = sms;
+        d.checked = true;
+    }
+    *dev_out = dev;
+    *sm_count = d.sm_count;
+    return d.status;
+}
+
+bool aligned(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+struct Range {
+    uintptr_t lo = 0, hi = 0;  // [lo, hi); empty when lo == hi
+};
+
+Range bytes_of(const void *p, size_t n) {
+    Range r;
+    if (p != nullptr && n > 0) {
+        r.lo = reinterpret_cast<uintptr_t>(p);
+        r.hi = r.lo + n;
+    }
+    return r;
+}
+
+Range matrix_of(const void *p, int64_t M, int64_t H, int64_t stride, int es) {
+    if (M <= 0) return Range{};
+    return bytes_of(p, (size_t)((M - 1) * stride + H) * (size_t)es);
+}
+
+bool overlap(const Range &a, const Range &b) {
+    return a.lo != a.hi && b.lo != b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+// Common shape checks; also rules out int64 overflow of the largest offset.
+int check_shape(int64_t M, int64_t H, int64_t stride, int dtype) {
+    if (dtype != RMSN_F32 && dtype != RMSN_F16 && dtype != RMSN_BF16) return RMSN_ERR_INVALID;
+    if (M < 0 || H <= 0 || H > kMaxH || stride < H) return RMSN_ERR_INVALID;
+    const int es = elem_bytes(dtype);
+    if (M > 0 && (M - 1) > (INT64_MAX / es - H) / stride) return RMSN_ERR_INVALID;
+    if (M > INT32_MAX) return RMSN_ERR_INVALID;  // grid arithmetic
+    return RMSN_OK;
+}
+
+bool rows_vectorisable(int64_t H, int64_t stride, int dtype) {
+    const int es = elem_bytes(dtype);
+    return (H * es) % 16 == 0 && (stride * es) % 16 == 0;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA; }
+
+int forward(const void *x, const void *residual, const void *weight, void *y, void *residual_out,
+            float *rrms, int64_t row_stride, int64_t M, int64_t H, float eps, int dtype, int has_weight,
+            void *stream, bool fused) {
+    int st = check_shape(M, H, row_stride, dtype);
+    if (st) return st;
+    if (!std::isfinite(eps) || eps < 0.0f) return RMSN_ERR_INVALID;
+    if (has_weight && weight == nullptr) return RMSN_ERR_INVALID;
+    if (M > 0) {  // with no rows the matrix pointers are never used
+        if (x == nullptr || y == nullptr) return RMSN_ERR_INVALID;
+        if (fused && (residual == nullptr || residual_out == nullptr)) return RMSN_ERR_INVALID;
+    }
+    const int es = elem_bytes(dtype);
+    const void *w = has_weight ? weight : nullptr;
+    for (const void *p : {x, residual, w, static_cast<const void *>(y), static_cast<const void *>(residual_out)})
+        if (p != nullptr && !aligned(p, es)) return RMSN_ERR_INVALID;
+    if (rrms != nullptr && !aligned(rrms, 4)) return RMSN_ERR_INVALID;
+
+    const Range rx = matrix_of(x, M, H, row_stride, es);
+    const Range rr = fused ? matrix_of(residual, M, H, row_stride, es) : Range{};
+    const Range rw = bytes_of(w, (size_t)H * es);
+    const Range ry = matrix_of(y, M, H, row_stride, es);
+    const Range rs = fused ? matrix_of(residual_out, M, H, row_stride, es) : Range{};
+    const Range rq = bytes_of(rrms, (size_t)M * sizeof(float));
+    const Range outs[] = {ry, rs, rq};
+    const Range all[] = {rx, rr, rw, ry, rs, rq};
+    for (int o = 0; o < 3; ++o)
+        for (int k = 0; k < 6; ++k)
+            if (k != 3 + o && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
+
+    if (M == 0) return RMSN_OK;
+    int dev = 0, sms = 0;
+    st = current_device(&dev, &sms);
+    if (st) return st;
+
+    bool vec = rows_vectorisable(H, row_stride, dtype);
+    for (const void *p : {x, residual, w, static_cast<const void *>(y), static_cast<const void *>(residual_out)})
+        if (p != nullptr && !aligned(p, 16)) vec = false;
+
+    FwdArgs a{};
+    a.x = x;
+    a.r = fused ? residual : nullptr;
+    a.w = w;
+    a.y = y;
+    a.s_out = fused ? residual_out : nullptr;
+    a.rrms = rrms;
+    a.stride = row_stride;
+    a.M = M;
+    a.H = (int)H;
+    a.eps = eps;
+    a.has_w = has_weight ? 1 : 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (H < kSmallH) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
+    if (fwd_row_fits((int)H, dtype, vec)) return to_status(launch_fwd_row(a, dtype, vec, sms, s));
+    return to_status(launch_fwd_chunked(a, dtype, vec, sms, s));
+}
+
+}  // namespace
+
+int occupancy(const void *func, int threads, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const auto key = std::make_tuple(dev, func, threads, smem);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_occ[key] = n;
+    return n;
+}
+
+}  // namespace rmsn
+
+using namespace rmsn;
+
+// the library is built with hidden visibility; only the C ABI is exported
+#define RMSN_API __attribute__((visibility("default")))
+
+extern "C" {
+
+RMSN_API int rmsnorm_fwd(const void *x, const void *weight, void *y, float *rrms, int64_t row_stride, int64_t M,
+                int64_t H, float eps, int dtype, int has_weight, void *stream) {
+    return forward(x, nullptr, weight, y, nullptr, rrms, row_stride, M, H, eps, dtype, has_weight, stream, false);
+}
+
+RMSN_API int rmsnorm_fwd_residual(const void *x, const void *residual, const void *weight, void *y, void *residual_out,
+                         float *rrms, int64_t row_stride, int64_t M, int64_t H, float eps, int dtype,
+                         int has_weight, void *stream) {
+    return forward(x, residual, weight, y, residual_out, rrms, row_stride, M, H, eps, dtype, has_weight, stream,
+                   true);
+}
+
+RMSN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype, size_t *bytes) {
+    if (bytes == nullptr) return RMSN_ERR_INVALID;
+    *bytes = 0;
+    int st = check_shape(M, H, H, dtype);
+    if (st) return st;
+    if (M == 0) return RMSN_OK;
+    int dev = 0, sms = 0;
+    st = current_device(&dev, &sms);
+    if (st) return st;
+    // the largest of the variants rmsnorm_bwd may pick for this shape
+    size_t need = bwd_partial_bytes(plan_bwd(M, (int)H, dtype, false, sms), (int)H);
+    if ((H * elem_bytes(dtype)) % 16 == 0) {
+        const size_t v = bwd_partial_bytes(plan_bwd(M, (int)H, dtype, true, sms), (int)H);
+        need = v > need ? v : need;
+    }
+    *bytes = need;
+    return RMSN_OK;
+}
+
+RMSN_API int rmsnorm_bwd(const void *dy, const void *x, const void *weight, const float *rrms, void *dx, float *dweight,
+                void *workspace, size_t workspace_bytes, int64_t row_stride, int64_t M, int64_t H, int dtype,
+                int has_weight, void *stream) {
+    int st = check_shape(M, H, row_stride, dtype);
+    if (st) return st;
+    if (has_weight && weight == nullptr) return RMSN_ERR_INVALID;
+    if (M > 0 && (dy == nullptr || x == nullptr || rrms == nullptr || dx == nullptr))
+        return RMSN_ERR_INVALID;  // with no rows the row pointers are never used
+    const int es = elem_bytes(dtype);
+    const void *w = has_weight ? weight : nullptr;
+    float *dw = has_weight ? dweight : nullptr;
+    for (const void *p : {dy, x, w, static_cast<const void *>(dx)})
+        if (p != nullptr && !aligned(p, es)) return RMSN_ERR_INVALID;
+    if ((rrms != nullptr && !aligned(rrms, 4)) || (dw != nullptr && !aligned(dw, 4))) return RMSN_ERR_INVALID;
+
+    if (M == 0) {
+        // no rows: dweight is an empty sum
+        if (dw != nullptr) return to_status(cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float),
+                                                            static_cast<cudaStream_t>(stream)));
+        return RMSN_OK;
+    }
+    int dev = 0, sms = 0;
+    st = current_device(&dev, &sms);
+    if (st) return st;
+
+    bool vec = rows_vectorisable(H, row_stride, dtype);
+    for (const void *p : {dy, x, w, static_cast<const void *>(dx)})
+        if (p != nullptr && !aligned(p, 16)) vec = false;
+    const BwdPlan plan = plan_bwd(M, (int)H, dtype, vec, sms);
+    const size_t part_bytes = dw != nullptr ? bwd_partial_bytes(plan, (int)H) : 0;
+    if (dw != nullptr) {
+        if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < part_bytes)
+            return RMSN_ERR_WORKSPACE;
+    }
+
+    const Range rdy = matrix_of(dy, M, H, row_stride, es);
+    const Range rx = matrix_of(x, M, H, row_stride, es);
+    const Range rw = bytes_of(w, (size_t)H * es);
+    const Range rq = bytes_of(rrms, (size_t)M * sizeof(float));
+    const Range rdx = matrix_of(dx, M, H, row_stride, es);
+    const Range rdw = bytes_of(dw, (size_t)H * sizeof(float));
+    const Range rws = bytes_of(dw != nullptr ? workspace : nullptr, part_bytes);
+    const Range outs[] = {rdx, rdw, rws};
+    const Range all[] = {rdy, rx, rw, rq, rdx, rdw, rws};
+    for (int o = 0; o < 3; ++o)
+        for (int k = 0; k < 7; ++k)
+            if (k != 4 + o && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
+
+    BwdArgs a{};
+    a.dy = dy;
+    a.x = x;
+    a.w = w;
+    a.rrms = rrms;
+    a.dx = dx;
+    a.partial = dw != nullptr ? static_cast<float *>(workspace) : nullptr;
+    a.stride = row_stride;
+    a.M = M;
+    a.H = (int)H;
+    a.has_w = has_weight ? 1 : 0;
+    return to_status(launch_bwd(a, plan, dtype, vec, dw, static_cast<cudaStream_t>(stream)));
+}
+
+RMSN_API const char *rmsnorm_status_string(int status) {
+    switch (status) {
+    case RMSN_OK: return "ok";
+    case RMSN_ERR_INVALID: return "invalid argument (pointer, size, stride, eps, dtype or alignment)";
+    case RMSN_ERR_ALIAS: return "an output overlaps another argument";
+    case RMSN_ERR_WORKSPACE: return "backward workspace missing, misaligned or too small";
+    case RMSN_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+    case RMSN_ERR_UNSUPPORTED: return "no usable sm_103 device is current";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

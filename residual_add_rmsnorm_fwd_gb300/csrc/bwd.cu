@@ -1,0 +1,312 @@
+// bwd.cu -- RMSNorm backward: dx per row, and a deterministic dweight.
+//
+// ("Skill: Write a Triton RMSNorm Kernel", Required reasoning 12;
+// Correctness requirements on the saved rrms and the dweight axis.)
+// With g = dy * w and xhat = x * rrms (rrms read from the forward's saved
+// buffer, never recomputed):
+//     dx      = rrms * (g - xhat * (sum_h g_h * xhat_h) / H)
+//     dweight = sum over rows of dy * xhat
+//
+// dweight is a cross-row reduction, so it is done in two launches with no
+// atomics and no inter-CTA waiting:
+//   1. a persistent grid of G CTAs; CTA b owns the rows b, b + G, b + 2G, ...
+//      and accumulates dy * xhat for its rows in binary32, column by column,
+//      then writes its partial sums to row b of a G x H workspace;
+//   2. a column kernel sums the G partials of each column in a fixed order.
+// The row-to-CTA assignment and both summation orders depend only on (M, H,
+// dtype, device), so dweight is bit-reproducible run to run.
+#include "launch.h"
+
+namespace rmsn {
+
+// Row kept in registers: a thread owns NV groups of VEC columns; its
+// dweight partials for those columns stay in registers across all its rows.
+template <typename T, int VEC, int NV>
+__global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
+    using P = Pack<T, VEC>;
+    __shared__ float red[64];
+    const T *__restrict__ dy = static_cast<const T *>(a.dy);
+    const T *__restrict__ x = static_cast<const T *>(a.x);
+    const T *__restrict__ w = static_cast<const T *>(a.w);
+    T *__restrict__ dx = static_cast<T *>(a.dx);
+    const int nvec = a.H / VEC;
+    const float hf = (float)a.H;
+
+    P wp[NV];
+    float acc[NV][VEC];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        wp[i] = (a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc[i][j] = 0.0f;
+    }
+
+    int bank = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const int64_t base = row * a.stride;
+        const float rr = __ldg(a.rrms + row);
+        P gp[NV], xp[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+                gp[i] = ld_stream<T, VEC>(dy + base + (int64_t)c * VEC);
+                xp[i] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
+            }
+        }
+        float dot = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const float d = to_f32(gp[i].v[j]);
+                    const float xh = to_f32(xp[i].v[j]) * rr;
+                    dot += (d * to_f32(wp[i].v[j])) * xh;
+                    acc[i][j] += d * xh;
+                }
+            }
+        }
+        const float c_row = block_sum(dot, red, bank) / hf;
+        bank ^= 1;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+                P o;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const float g = to_f32(gp[i].v[j]) * to_f32(wp[i].v[j]);
+                    const float xh = to_f32(xp[i].v[j]) * rr;
+                    o.v[j] = from_f32<T>(rr * (g - xh * c_row));
+                }
+                st_global<T, VEC>(dx + base + (int64_t)c * VEC, o);
+            }
+        }
+    }
+
+    if (a.partial != nullptr) {
+        float *prow = a.partial + (int64_t)blockIdx.x * a.H;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+                if constexpr (VEC % 4 == 0) {
+#pragma unroll
+                    for (int j = 0; j < VEC; j += 4)
+                        *reinterpret_cast<float4 *>(prow + (int64_t)c * VEC + j) =
+                            make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) prow[(int64_t)c * VEC + j] = acc[i][j];
+                }
+            }
+        }
+    }
+}
+
+// H above the register budget: two passes over each row with identical chunk
+// bounds.  The CTA's dweight partial row lives in the workspace; it belongs
+// to this CTA alone, so it is updated with plain read-modify-write (the
+// first row of the CTA initialises it).
+template <typename T, int VEC>
+__global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
+    using P = Pack<T, VEC>;
+    constexpr int U = 2;
+    __shared__ float red[64];
+    const T *__restrict__ dy = static_cast<const T *>(a.dy);
+    const T *__restrict__ x = static_cast<const T *>(a.x);
+    const T *__restrict__ w = static_cast<const T *>(a.w);
+    T *__restrict__ dx = static_cast<T *>(a.dx);
+    const int nvec = a.H / VEC;
+    const float hf = (float)a.H;
+    const int chunk = blockDim.x * U;
+    float *prow = a.partial != nullptr ? a.partial + (int64_t)blockIdx.x * a.H : nullptr;
+
+    int bank = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const int64_t base = row * a.stride;
+        const float rr = __ldg(a.rrms + row);
+        const bool first = row == blockIdx.x;
+        float dot = 0.0f;
+        for (int c0 = 0; c0 < nvec; c0 += chunk) {
+            P gp[U], xp[U], wp[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * blockDim.x + threadIdx.x;
+                if (c < nvec) {
+                    gp[u] = ld_cached<T, VEC>(dy + base + (int64_t)c * VEC);
+                    xp[u] = ld_cached<T, VEC>(x + base + (int64_t)c * VEC);
+                    wp[u] = a.has_w ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * blockDim.x + threadIdx.x;
+                if (c < nvec) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        dot += (to_f32(gp[u].v[j]) * to_f32(wp[u].v[j])) * (to_f32(xp[u].v[j]) * rr);
+                }
+            }
+        }
+        const float c_row = block_sum(dot, red, bank) / hf;
+        bank ^= 1;
+        for (int c0 = 0; c0 < nvec; c0 += chunk) {
+            P gp[U], xp[U], wp[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * blockDim.x + threadIdx.x;
+                if (c < nvec) {
+                    gp[u] = ld_stream<T, VEC>(dy + base + (int64_t)c * VEC);
+                    xp[u] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
+                    wp[u] = a.has_w ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * blockDim.x + threadIdx.x;
+                if (c < nvec) {
+                    P o;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const float d = to_f32(gp[u].v[j]);
+                        const float xh = to_f32(xp[u].v[j]) * rr;
+                        o.v[j] = from_f32<T>(rr * (d * to_f32(wp[u].v[j]) - xh * c_row));
+                        if (prow != nullptr) {
+                            float *p = prow + (int64_t)c * VEC + j;
+                            *p = first ? d * xh : *p + d * xh;
+                        }
+                    }
+                    st_global<T, VEC>(dx + base + (int64_t)c * VEC, o);
+                }
+            }
+        }
+    }
+}
+
+// dweight_h = sum_{b = 0}^{G-1} partial[b][h].  A CTA covers 32 columns with
+// 8 warps; warp k sums the contiguous slice of partial rows
+// [k*G/8, (k+1)*G/8) in ascending order, then the 8 slice sums are added in
+// ascending k.  Fixed order, so the result is reproducible.
+__global__ void __launch_bounds__(256) dweight_reduce_kernel(const float *__restrict__ partial, int G, int H,
+                                                             float *__restrict__ dweight) {
+    __shared__ float part[8][33];
+    const int col = threadIdx.x & 31, k = threadIdx.x >> 5;
+    const int h = blockIdx.x * 32 + col;
+    float s = 0.0f;
+    if (h < H) {
+        const int g0 = (int)((int64_t)G * k / 8), g1 = (int)((int64_t)G * (k + 1) / 8);
+        for (int g = g0; g < g1; ++g) s += __ldg(partial + (int64_t)g * H + h);
+    }
+    part[k][col] = s;
+    __syncthreads();
+    if (k == 0 && h < H) {
+        float t = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t += part[q][col];
+        dweight[h] = t;
+    }
+}
+
+namespace {
+
+constexpr int kRowMaxThreads = 512;
+constexpr int kChunkThreads = 512;
+constexpr int kVecNV[] = {1, 2};
+constexpr int kScalarNV[] = {1, 2, 4, 8};
+
+inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+bool pick_row(int nvec, bool vec, int &threads, int &nv) {
+    const int *set = vec ? kVecNV : kScalarNV;
+    const int n = vec ? 2 : 4;
+    for (int k = 0; k < n; ++k) {
+        const int t = round_up((nvec + set[k] - 1) / set[k], 32);
+        if (t <= kRowMaxThreads) {
+            threads = t;
+            nv = set[k];
+            return true;
+        }
+    }
+    return false;
+}
+
+template <typename T, int VEC, int NV>
+const void *row_kernel() {
+    return reinterpret_cast<const void *>(bwd_row_kernel<T, VEC, NV>);
+}
+
+template <typename T>
+const void *row_kernel_for(bool vec, int nv) {
+    constexpr int V = Vec16<T>::n;
+    if (vec) {
+        switch (nv) {
+        case 1: return row_kernel<T, V, 1>();
+        case 2: return row_kernel<T, V, 2>();
+        }
+    } else {
+        switch (nv) {
+        case 1: return row_kernel<T, 1, 1>();
+        case 2: return row_kernel<T, 1, 2>();
+        case 4: return row_kernel<T, 1, 4>();
+        case 8: return row_kernel<T, 1, 8>();
+        }
+    }
+    return nullptr;
+}
+
+template <typename T>
+const void *chunked_kernel_for(bool vec) {
+    constexpr int V = Vec16<T>::n;
+    return vec ? reinterpret_cast<const void *>(bwd_chunked_kernel<T, V>)
+               : reinterpret_cast<const void *>(bwd_chunked_kernel<T, 1>);
+}
+
+const void *kernel_for(const BwdPlan &p, int dtype, bool vec) {
+    switch (dtype) {
+    case kF32: return p.row ? row_kernel_for<float>(vec, p.nv) : chunked_kernel_for<float>(vec);
+    case kF16: return p.row ? row_kernel_for<__half>(vec, p.nv) : chunked_kernel_for<__half>(vec);
+    case kBF16:
+        return p.row ? row_kernel_for<__nv_bfloat16>(vec, p.nv) : chunked_kernel_for<__nv_bfloat16>(vec);
+    }
+    return nullptr;
+}
+
+}  // namespace
+
+BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, int sm_count) {
+    BwdPlan p{};
+    const int nvec = vec ? H / vec_elems(dtype) : H;
+    p.row = pick_row(nvec, vec, p.threads, p.nv);
+    if (!p.row) {
+        p.threads = kChunkThreads;
+        p.nv = 0;
+    }
+    const void *k = kernel_for(p, dtype, vec);
+    const int occ = k ? occupancy(k, p.threads, 0) : 0;
+    const int64_t cap = (int64_t)(occ > 0 ? occ : 1) * sm_count;
+    p.grid = (int)(M < cap ? (M > 0 ? M : 1) : cap);
+    return p;
+}
+
+size_t bwd_partial_bytes(const BwdPlan &p, int H) { return (size_t)p.grid * (size_t)H * sizeof(float); }
+
+cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, float *dweight,
+                       cudaStream_t st) {
+    const void *k = kernel_for(p, dtype, vec);
+    if (k == nullptr) return cudaErrorInvalidValue;
+    BwdArgs args = a;
+    void *params[] = {&args};
+    cudaError_t e = cudaLaunchKernel(k, dim3((unsigned)p.grid), dim3((unsigned)p.threads), params, 0, st);
+    if (e != cudaSuccess) return e;
+    if (dweight != nullptr && a.partial != nullptr) {
+        dweight_reduce_kernel<<<(unsigned)((a.H + 31) / 32), 256, 0, st>>>(a.partial, p.grid, a.H, dweight);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+}  // namespace rmsn

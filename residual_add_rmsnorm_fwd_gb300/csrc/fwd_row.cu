@@ -1,0 +1,175 @@
+// fwd_row.cu -- RMSNorm forward (plain and residual-fused) for hidden sizes
+// whose row fits in the registers of one CTA.
+//
+// One CTA per row, persistent: the grid holds as many CTAs as fit on the
+// device and each CTA strides over rows.  A thread owns NV fixed column
+// groups of VEC elements (128-bit accesses when the layout allows, else
+// single elements), so the weight is loaded into registers once per CTA and
+// the row stays in registers between the binary32 sum of squares and the
+// scale step: x (and the residual) are read from HBM exactly once
+// ("Skill: Write a Triton RMSNorm Kernel", Required reasoning 3; Performance
+// requirements, persistent vs two-pass).
+#include "launch.h"
+
+namespace rmsn {
+
+template <typename T, int VEC, int NV, bool RESID>
+__global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
+    using P = Pack<T, VEC>;
+    __shared__ float red[64];
+    const T *__restrict__ x = static_cast<const T *>(a.x);
+    const T *__restrict__ r = static_cast<const T *>(a.r);
+    const T *__restrict__ w = static_cast<const T *>(a.w);
+    T *__restrict__ y = static_cast<T *>(a.y);
+    T *__restrict__ s_out = static_cast<T *>(a.s_out);
+    const int nvec = a.H / VEC;
+    const float hf = (float)a.H;   // exact: H < 2^24
+
+    // weight (H,), indexed by column only; ones when the norm has no weight
+    P wp[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        wp[i] = (a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+    }
+
+    int bank = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const int64_t base = row * a.stride;
+        P xp[NV], rp[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+                xp[i] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
+                if constexpr (RESID) rp[i] = ld_stream<T, VEC>(r + base + (int64_t)c * VEC);
+            }
+        }
+        // binary32 sum of squares (residual added in binary32 first); the
+        // post-add sum is written back as the next residual stream
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+                P so;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    float s = to_f32(xp[i].v[j]);
+                    if constexpr (RESID) {
+                        s += to_f32(rp[i].v[j]);
+                        so.v[j] = from_f32<T>(s);
+                    }
+                    ss += s * s;
+                }
+                if constexpr (RESID) st_global<T, VEC>(s_out + base + (int64_t)c * VEC, so);
+            }
+        }
+        const float total = block_sum(ss, red, bank);
+        bank ^= 1;
+        // mean over the full row length, eps inside the square root
+        const float rrms = rsqrtf(total / hf + a.eps);
+        if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[row] = rrms;
+        // y = (s * rrms) * w, one rounding to the storage type
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+                P yo;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    float s = to_f32(xp[i].v[j]);
+                    if constexpr (RESID) s += to_f32(rp[i].v[j]);
+                    yo.v[j] = from_f32<T>((s * rrms) * to_f32(wp[i].v[j]));
+                }
+                st_global<T, VEC>(y + base + (int64_t)c * VEC, yo);
+            }
+        }
+    }
+}
+
+namespace {
+
+constexpr int kMaxThreads = 512;
+constexpr int kVecNV[] = {1, 2, 3, 4};
+constexpr int kScalarNV[] = {1, 2, 4, 8, 16};
+
+inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// Smallest NV (from the instantiated set) whose thread count fits a CTA.
+bool pick(int nvec, bool vec, int &threads, int &nv) {
+    const int *set = vec ? kVecNV : kScalarNV;
+    const int n = vec ? 4 : 5;
+    for (int k = 0; k < n; ++k) {
+        const int t = round_up((nvec + set[k] - 1) / set[k], 32);
+        if (t <= kMaxThreads) {
+            threads = t;
+            nv = set[k];
+            return true;
+        }
+    }
+    return false;
+}
+
+template <typename T, int VEC, int NV, bool RESID>
+cudaError_t launch_t(const FwdArgs &a, int threads, int sm_count, cudaStream_t st) {
+    auto k = fwd_row_kernel<T, VEC, NV, RESID>;
+    const int occ = occupancy(reinterpret_cast<const void *>(k), threads, 0);
+    if (occ <= 0) return cudaErrorInvalidConfiguration;
+    const int64_t grid = a.M < (int64_t)occ * sm_count ? a.M : (int64_t)occ * sm_count;
+    k<<<(unsigned)grid, threads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int VEC, bool RESID>
+cudaError_t launch_nv(const FwdArgs &a, int nv, int threads, int sm_count, cudaStream_t st) {
+    if constexpr (VEC > 1) {
+        switch (nv) {
+        case 1: return launch_t<T, VEC, 1, RESID>(a, threads, sm_count, st);
+        case 2: return launch_t<T, VEC, 2, RESID>(a, threads, sm_count, st);
+        case 3: return launch_t<T, VEC, 3, RESID>(a, threads, sm_count, st);
+        case 4: return launch_t<T, VEC, 4, RESID>(a, threads, sm_count, st);
+        }
+    } else {
+        switch (nv) {
+        case 1: return launch_t<T, 1, 1, RESID>(a, threads, sm_count, st);
+        case 2: return launch_t<T, 1, 2, RESID>(a, threads, sm_count, st);
+        case 4: return launch_t<T, 1, 4, RESID>(a, threads, sm_count, st);
+        case 8: return launch_t<T, 1, 8, RESID>(a, threads, sm_count, st);
+        case 16: return launch_t<T, 1, 16, RESID>(a, threads, sm_count, st);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t launch_dt(const FwdArgs &a, bool vec, int sm_count, cudaStream_t st) {
+    constexpr int V = Vec16<T>::n;
+    int threads = 0, nv = 0;
+    if (!pick(vec ? a.H / V : a.H, vec, threads, nv)) return cudaErrorInvalidValue;
+    const bool resid = a.r != nullptr;
+    if (vec) {
+        return resid ? launch_nv<T, V, true>(a, nv, threads, sm_count, st)
+                     : launch_nv<T, V, false>(a, nv, threads, sm_count, st);
+    }
+    return resid ? launch_nv<T, 1, true>(a, nv, threads, sm_count, st)
+                 : launch_nv<T, 1, false>(a, nv, threads, sm_count, st);
+}
+
+}  // namespace
+
+bool fwd_row_fits(int H, int dtype, bool vec) {
+    int threads, nv;
+    return pick(vec ? H / vec_elems(dtype) : H, vec, threads, nv);
+}
+
+cudaError_t launch_fwd_row(const FwdArgs &a, int dtype, bool vec, int sm_count, cudaStream_t st) {
+    switch (dtype) {
+    case kF32: return launch_dt<float>(a, vec, sm_count, st);
+    case kF16: return launch_dt<__half>(a, vec, sm_count, st);
+    case kBF16: return launch_dt<__nv_bfloat16>(a, vec, sm_count, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rmsn

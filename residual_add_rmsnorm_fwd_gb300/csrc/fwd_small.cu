@@ -1,0 +1,149 @@
+// fwd_small.cu -- RMSNorm forward (plain and residual-fused) for small hidden
+// sizes (H below 256), such as the per-head norm at H = 64.
+//
+// A whole CTA per row would leave most threads idle and pay a CTA-wide
+// barrier per row, so each row is handled by an aligned group of LANES lanes
+// of one warp (LANES = 1..32, the smallest power of two covering the row's
+// 128-bit vectors, or its elements on the scalar path).  A warp processes
+// 32 / LANES rows at once and reduces each row with xor shuffles that stay
+// inside its lane group: no shared memory, no barrier.  (The page advises
+// warp-level reductions for hidden sizes below 256: "Skill: Write a Triton
+// RMSNorm Kernel", Do not use this when, third bullet.)
+#include "launch.h"
+
+namespace rmsn {
+
+template <typename T, int VEC, int LANES, int NPL, bool RESID>
+__global__ void __launch_bounds__(256) fwd_small_kernel(FwdArgs a) {
+    using P = Pack<T, VEC>;
+    constexpr int RPW = 32 / LANES;  // rows per warp
+    const T *__restrict__ x = static_cast<const T *>(a.x);
+    const T *__restrict__ r = static_cast<const T *>(a.r);
+    const T *__restrict__ w = static_cast<const T *>(a.w);
+    T *__restrict__ y = static_cast<T *>(a.y);
+    T *__restrict__ s_out = static_cast<T *>(a.s_out);
+    const int nvec = a.H / VEC;
+    const float hf = (float)a.H;
+    const int lane = threadIdx.x & 31;
+    const int slot = lane / LANES;   // which of the warp's rows
+    const int li = lane % LANES;     // lane within the row's group
+
+    P wp[NPL];
+#pragma unroll
+    for (int k = 0; k < NPL; ++k) {
+        const int c = li + k * LANES;
+        wp[k] = (a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+    }
+
+    const int64_t warps_per_grid = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t warp_id = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    // warp-uniform loop: every lane takes part in the shuffles
+    for (int64_t row0 = warp_id * RPW; row0 < a.M; row0 += warps_per_grid * RPW) {
+        const int64_t row = row0 + slot;
+        const bool live = row < a.M;
+        const int64_t base = row * a.stride;
+        P xp[NPL], rp[NPL];
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) {
+            const int c = li + k * LANES;
+            if (live && c < nvec) {
+                xp[k] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
+                if constexpr (RESID) rp[k] = ld_stream<T, VEC>(r + base + (int64_t)c * VEC);
+            }
+        }
+        float ss = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) {
+            const int c = li + k * LANES;
+            if (live && c < nvec) {
+                P so;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    float s = to_f32(xp[k].v[j]);
+                    if constexpr (RESID) {
+                        s += to_f32(rp[k].v[j]);
+                        so.v[j] = from_f32<T>(s);
+                    }
+                    ss += s * s;
+                }
+                if constexpr (RESID) st_global<T, VEC>(s_out + base + (int64_t)c * VEC, so);
+            }
+        }
+        const float total = group_sum<LANES>(ss);
+        const float rrms = rsqrtf(total / hf + a.eps);
+        if (live && li == 0 && a.rrms != nullptr) a.rrms[row] = rrms;
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) {
+            const int c = li + k * LANES;
+            if (live && c < nvec) {
+                P yo;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    float s = to_f32(xp[k].v[j]);
+                    if constexpr (RESID) s += to_f32(rp[k].v[j]);
+                    yo.v[j] = from_f32<T>((s * rrms) * to_f32(wp[k].v[j]));
+                }
+                st_global<T, VEC>(y + base + (int64_t)c * VEC, yo);
+            }
+        }
+    }
+}
+
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T, int VEC, int LANES, int NPL, bool RESID>
+cudaError_t launch_t(const FwdArgs &a, int sm_count, cudaStream_t st) {
+    auto k = fwd_small_kernel<T, VEC, LANES, NPL, RESID>;
+    const int occ = occupancy(reinterpret_cast<const void *>(k), kThreads, 0);
+    if (occ <= 0) return cudaErrorInvalidConfiguration;
+    constexpr int rows_per_cta = (kThreads / 32) * (32 / LANES);
+    const int64_t need = (a.M + rows_per_cta - 1) / rows_per_cta;
+    const int64_t cap = (int64_t)occ * sm_count;
+    k<<<(unsigned)(need < cap ? need : cap), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int VEC, bool RESID>
+cudaError_t launch_shape(const FwdArgs &a, int n, int sm_count, cudaStream_t st) {
+    // n = vectors (or elements) per row, 1..255
+    if (n <= 1) return launch_t<T, VEC, 1, 1, RESID>(a, sm_count, st);
+    if (n <= 2) return launch_t<T, VEC, 2, 1, RESID>(a, sm_count, st);
+    if (n <= 4) return launch_t<T, VEC, 4, 1, RESID>(a, sm_count, st);
+    if (n <= 8) return launch_t<T, VEC, 8, 1, RESID>(a, sm_count, st);
+    if (n <= 16) return launch_t<T, VEC, 16, 1, RESID>(a, sm_count, st);
+    if (n <= 32) return launch_t<T, VEC, 32, 1, RESID>(a, sm_count, st);
+    if (n <= 64) return launch_t<T, VEC, 32, 2, RESID>(a, sm_count, st);
+    if constexpr (VEC == 1) {
+        if (n <= 128) return launch_t<T, 1, 32, 4, RESID>(a, sm_count, st);
+        if (n <= 256) return launch_t<T, 1, 32, 8, RESID>(a, sm_count, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t launch_dt(const FwdArgs &a, bool vec, int sm_count, cudaStream_t st) {
+    constexpr int V = Vec16<T>::n;
+    const bool resid = a.r != nullptr;
+    if (vec) {
+        const int n = a.H / V;
+        return resid ? launch_shape<T, V, true>(a, n, sm_count, st)
+                     : launch_shape<T, V, false>(a, n, sm_count, st);
+    }
+    return resid ? launch_shape<T, 1, true>(a, a.H, sm_count, st)
+                 : launch_shape<T, 1, false>(a, a.H, sm_count, st);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_small(const FwdArgs &a, int dtype, bool vec, int sm_count, cudaStream_t st) {
+    switch (dtype) {
+    case kF32: return launch_dt<float>(a, vec, sm_count, st);
+    case kF16: return launch_dt<__half>(a, vec, sm_count, st);
+    case kBF16: return launch_dt<__nv_bfloat16>(a, vec, sm_count, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rmsn

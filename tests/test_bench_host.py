@@ -1,0 +1,88 @@
+"""Host-side logic of bench.py (no GPU): byte accounting, the clock-sample
+parser, whole-job aggregation, and the multi-rank max-over-ranks path run as
+two gloo ranks on the CPU."""
+import os
+import socket
+
+import pytest
+
+import bench
+
+
+def test_algorithmic_bytes_match_the_workload_table():
+    # fused forward, bf16, 16384 x 4096, no rrms: 4 tensors + weight
+    assert bench.step_bytes(16384, 4096, 2, fused=True, weight=True, save_rrms=False, backward=False)[0] \
+        == 536_879_104
+    # forward saving rrms, and backward, bf16 16384 x 8192
+    f, b = bench.step_bytes(16384, 8192, 2, fused=False, weight=True, save_rrms=True, backward=True)
+    assert f == 536_952_832 and b == 805_421_056
+    # fp16 fused forward + backward, 32768 x 6144 (padding excluded)
+    f, b = bench.step_bytes(32768, 6144, 2, fused=True, weight=True, save_rrms=True, backward=True)
+    assert f == 1_610_756_096 and b == 1_208_127_488
+
+
+def test_aggregate_uses_slowest_rank():
+    a = bench.aggregate([2.0, 4.0], units_per_rank=100, bytes_per_unit_rank=1e9)
+    assert a["ms"] == 4.0
+    assert a["units_per_s"] == pytest.approx(2 * 100 / 4e-3)
+    assert a["gbs"] == pytest.approx(2 * 1e9 / 4e-3 / 1e9)
+
+
+def test_clock_parser_and_summary():
+    lines = [
+        "2026/12/02 10:00:00.100, 0, 1965, 2070, 700.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:00.300, 0, 1980, 2070, 900.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "garbage line",
+    ]
+    rows = bench.parse_clock_lines(lines)
+    assert len(rows) == 2 and rows[1]["sw_power_cap"] and not rows[0]["sw_power_cap"]
+    t0 = rows[0]["t"]
+    s = bench.summarize_clocks(rows, t0, t0 + 1)
+    assert s["sm_mhz"] == pytest.approx(1972.5) and s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_profile_traffic_requires_matching_kernel_hash(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles" / "k.md").write_text(f"- kernel_source_hash: `{h}`\n- dram_bytes_per_launch: 123\n")
+    assert bench.profile_traffic("k") == 123
+    (tmp_path / "profiles" / "k.md").write_text("- kernel_source_hash: `other`\n- dram_bytes_per_launch: 123\n")
+    assert bench.profile_traffic("k") is None
+    assert bench.profile_traffic("missing") is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    per_rank_ms = [1.5, 3.0][rank]
+    all_ms = bench.max_over_ranks(per_rank_ms, world)
+    agg = bench.aggregate(all_ms, units_per_rank=16384, bytes_per_unit_rank=9.4e8)
+    bench.barrier(world)
+    dist.destroy_process_group()
+    q.put((rank, all_ms, agg))
+
+
+def test_two_rank_aggregation_gloo():
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, all_ms, agg in out:
+        assert sorted(all_ms) == [1.5, 3.0]
+        assert agg["ms"] == 3.0                                # slowest rank
+        assert agg["units_per_s"] == pytest.approx(2 * 16384 / 3e-3)
