@@ -65,7 +65,7 @@ def _load():
             lib.orc_decode.argtypes = [i32, p, p, i64]
             lib.orc_encode.argtypes = [i32, p, p, i64]
             lib.orc_rmsnorm_fwd.argtypes = [i32, p, p, p, i64, i64, i64, d, p, p, p, i32]
-            lib.orc_rmsnorm_bwd.argtypes = [i32, p, p, p, i64, i64, i64, d, p, p, p, p, i32]
+            lib.orc_rmsnorm_bwd.argtypes = [i32, p, p, p, i64, i64, i64, d, p, p, p, p, p, i32]
             for f in (lib.orc_decode, lib.orc_encode, lib.orc_rmsnorm_fwd, lib.orc_rmsnorm_bwd):
                 f.restype = i32
             _lib = lib
@@ -160,8 +160,11 @@ def rmsnorm_bwd(dy, x, w, eps: float, dtype: str, want_dx: bool = True,
                 want_dweight: bool = True, nthreads: int | None = None):
     """Backward on storage arrays; rrms is recomputed in binary64 from x.
 
-    Returns dict: ``dx`` (M, H) or None, ``dweight`` and ``dweight_abs`` (H,)
-    or None (``dweight_abs`` = sum over rows of |dy * xhat|), ``rrms`` (M,).
+    Returns dict: ``dx`` and ``dx_scale`` (M, H) or None, ``dweight`` and
+    ``dweight_abs`` (H,) or None, ``rrms`` (M,).  ``dx_scale`` is the size of
+    the two terms whose difference forms dx (|rrms*g| + |xhat*rrms/H| *
+    sum|g*xhat|); ``dweight_abs`` = sum over rows of |dy * xhat|.  Both bound
+    the rounding error of any evaluation order and scale the tolerances.
     """
     x, M, H, stride = _matrix(x, dtype, "x")
     dy, Md, Hd, sd = _matrix(dy, dtype, "dy")
@@ -177,12 +180,13 @@ def rmsnorm_bwd(dy, x, w, eps: float, dtype: str, want_dx: bool = True,
         if w.shape != (H,):
             raise ValueError("w must have shape (H,)")
     dx = np.empty((M, H), np.float64) if want_dx else None
+    dx_scale = np.empty((M, H), np.float64) if want_dx else None
     dweight = np.empty((H,), np.float64) if want_dweight else None
     dweight_abs = np.empty((H,), np.float64) if want_dweight else None
     rrms = np.empty((M,), np.float64)
     rc = _load().orc_rmsnorm_bwd(DTYPES[dtype], _ptr(dy), _ptr(x), _ptr(w), M, H, stride,
-                                 eps_as_f32(eps), _ptr(dx), _ptr(dweight), _ptr(dweight_abs),
-                                 _ptr(rrms), nthreads or default_threads())
+                                 eps_as_f32(eps), _ptr(dx), _ptr(dx_scale), _ptr(dweight),
+                                 _ptr(dweight_abs), _ptr(rrms), nthreads or default_threads())
     if rc:
         raise ValueError(f"orc_rmsnorm_bwd failed ({rc})")
-    return {"dx": dx, "dweight": dweight, "dweight_abs": dweight_abs, "rrms": rrms}
+    return {"dx": dx, "dx_scale": dx_scale, "dweight": dweight, "dweight_abs": dweight_abs, "rrms": rrms}

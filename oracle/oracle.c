@@ -298,7 +298,7 @@ struct bwd_ctx {
     const void *dy, *x, *w;
     int64_t M, H, stride;
     double eps;
-    double *dx, *dweight, *dweight_abs, *rrms;
+    double *dx, *dx_scale, *dweight, *dweight_abs, *rrms;
 };
 
 /* rrms per row, recomputed in binary64 from the stored input row */
@@ -315,7 +315,11 @@ static void bwd_rrms_rows(void *p, int64_t i0, int64_t i1)
     }
 }
 
-/* dx_h = rrms*g_h - xhat_h*(rrms/H)*sum_k g_k*xhat_k, g = dy*w, xhat = x*rrms */
+/* dx_h = rrms*g_h - xhat_h*(rrms/H)*sum_k g_k*xhat_k, g = dy*w, xhat = x*rrms.
+   dx_scale_h = |rrms*g_h| + |xhat_h*(rrms/H)| * sum_k |g_k*xhat_k| is the size
+   of the two terms whose difference is dx_h: the rounding error of any
+   binary32 evaluation of dx_h is a small multiple of u * dx_scale_h, even
+   where the difference cancels (H = 1, or x parallel to g). */
 static void bwd_dx_rows(void *p, int64_t i0, int64_t i1)
 {
     const struct bwd_ctx *c = (const struct bwd_ctx *)p;
@@ -323,18 +327,21 @@ static void bwd_dx_rows(void *p, int64_t i0, int64_t i1)
     for (int64_t i = i0; i < i1; ++i) {
         const int64_t row = i * c->stride;
         const double rrms = c->rrms[i];
-        double dot = 0.0;
+        double dot = 0.0, dot_abs = 0.0;
         for (int64_t h = 0; h < H; ++h) {
             double w = c->w ? load_elem(c->dtype, c->w, h) : 1.0;
             double g = load_elem(c->dtype, c->dy, row + h) * w;
             double xhat = load_elem(c->dtype, c->x, row + h) * rrms;
             dot += g * xhat;
+            dot_abs += fabs(g * xhat);
         }
         for (int64_t h = 0; h < H; ++h) {
             double w = c->w ? load_elem(c->dtype, c->w, h) : 1.0;
             double g = load_elem(c->dtype, c->dy, row + h) * w;
             double xhat = load_elem(c->dtype, c->x, row + h) * rrms;
             c->dx[i * H + h] = rrms * g - xhat * (rrms / (double)H) * dot;
+            if (c->dx_scale)
+                c->dx_scale[i * H + h] = fabs(rrms * g) + fabs(xhat * (rrms / (double)H)) * dot_abs;
         }
     }
 }
@@ -372,14 +379,15 @@ static void bwd_dweight_cols(void *p, int64_t h0, int64_t h1)
 
 /*
  * dy, x storage arrays with row stride `stride`; w nullable (no weight: g = dy).
- * Outputs (all nullable): dx dense M x H binary64, dweight and dweight_abs H
- * binary64, rrms M binary64 (recomputed from x; scratch is allocated here if
- * the caller passes NULL).
+ * Outputs (all nullable): dx and dx_scale dense M x H binary64 (dx_scale is
+ * only written together with dx), dweight and dweight_abs H binary64, rrms M
+ * binary64 (recomputed from x; scratch is allocated here if the caller passes
+ * NULL).
  */
 int orc_rmsnorm_bwd(int dtype, const void *dy, const void *x, const void *w,
                     int64_t M, int64_t H, int64_t stride, double eps,
-                    double *dx, double *dweight, double *dweight_abs, double *rrms,
-                    int nthreads)
+                    double *dx, double *dx_scale, double *dweight, double *dweight_abs,
+                    double *rrms, int nthreads)
 {
     if (!elem_size(dtype) || !dy || !x || M < 0 || H <= 0 || stride < H)
         return 1;
@@ -389,7 +397,7 @@ int orc_rmsnorm_bwd(int dtype, const void *dy, const void *x, const void *w,
         if (!rr)
             return 2;
     }
-    struct bwd_ctx c = {dtype, dy, x, w, M, H, stride, eps, dx, dweight, dweight_abs, rr};
+    struct bwd_ctx c = {dtype, dy, x, w, M, H, stride, eps, dx, dx_scale, dweight, dweight_abs, rr};
     parallel_ranges(bwd_rrms_rows, &c, M, nthreads);
     if (dx)
         parallel_ranges(bwd_dx_rows, &c, M, nthreads);

@@ -82,10 +82,13 @@ def check_fwd_values(got_bits: np.ndarray, ref64: np.ndarray, dtype: str, oracle
     return {"failed": int(bad.sum()), "max_err": float(err.max()) if err.size else 0.0, "bad": bad}
 
 
-def check_rows_rel(got: np.ndarray, ref: np.ndarray, rtol: float) -> dict:
-    """Backward dx tolerance per element: |got - ref| <= rtol * max(|ref|, rms of the ref row)."""
+def check_dx(got: np.ndarray, ref: np.ndarray, scale: np.ndarray, rtol: float) -> dict:
+    """Backward dx tolerance per element:
+    |got - ref| <= rtol * max(|ref|, rms of the ref row, dx_scale), where
+    dx_scale is the oracle's size of the two terms whose difference is dx
+    (rounding error of any binary32 evaluation is proportional to it)."""
     row_rms = np.sqrt(np.mean(ref * ref, axis=1, keepdims=True))
-    denom = np.maximum(np.abs(ref), row_rms)
+    denom = np.maximum(np.maximum(np.abs(ref), row_rms), scale)
     err = np.abs(got - ref)
     bad = ~(err <= rtol * denom)
     return {"failed": int(bad.sum()), "max_rel": float((err / np.where(denom > 0, denom, 1)).max())

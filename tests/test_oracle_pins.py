@@ -256,3 +256,22 @@ def test_backward_rrms_matches_forward(oracle):
     f = oracle.rmsnorm_fwd(x, None, 1e-5, "f32")
     b = oracle.rmsnorm_bwd(np.ones_like(x), x, None, 1e-5, "f32", want_dx=False, want_dweight=False)
     assert np.array_equal(f["rrms"], b["rrms"])
+
+
+def test_dx_scale_bounds_dx_and_single_column_form(oracle):
+    """dx_scale = |rrms g| + |xhat rrms / H| sum|g xhat| >= |dx|; for H = 1 it is rrms |g| (1 + xhat^2)
+    while dx = rrms g (1 - xhat^2) = rrms g eps / (x^2 + eps)."""
+    rng = np.random.default_rng(25)
+    x = rng.standard_normal((7, 1))
+    dy = rng.standard_normal((7, 1))
+    w = np.array([0.8])
+    eps = 1e-3
+    e = oracle.eps_as_f32(eps)
+    out = oracle.rmsnorm_bwd(dy, x, w, eps, "f64")
+    rrms = 1 / np.sqrt(x[:, 0] ** 2 + e)
+    xh = x[:, 0] * rrms
+    g = dy[:, 0] * 0.8
+    np.testing.assert_allclose(out["dx_scale"][:, 0], rrms * np.abs(g) * (1 + xh ** 2), rtol=1e-14)
+    np.testing.assert_allclose(out["dx"][:, 0], rrms * g * e / (x[:, 0] ** 2 + e), rtol=1e-9)
+    big = oracle.rmsnorm_bwd(rng.standard_normal((5, 40)), rng.standard_normal((5, 40)), None, eps, "f64")
+    assert np.all(big["dx_scale"] >= np.abs(big["dx"]))
