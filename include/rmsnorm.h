@@ -35,7 +35,7 @@
  *     surface at the caller's next synchronisation.
  *   - All arguments are validated before anything is launched.  An invalid
  *     call returns a nonzero rmsn_status and launches nothing.  M == 0 is a
- *     valid no-op.
+ *     valid no-op (row pointers and rrms may then be NULL).
  *   - An output may not overlap any other argument (byte ranges of the rows
  *     [0, M) are compared): in-place use is rejected with RMSN_ERR_ALIAS.
  */
@@ -133,6 +133,16 @@ int rmsnorm_bwd(const void *dy, const void *x, const void *weight, const float *
                 void *dx, float *dweight, void *workspace, size_t workspace_bytes,
                 int64_t row_stride, int64_t M, int64_t H,
                 int dtype, int has_weight, void *stream);
+
+/*
+ * Device-side error flags of the current device, read and cleared.
+ * Synchronises the device first.  Bit 0 (RMSN_DEVERR_PIPELINE_TIMEOUT): a
+ * kernel's bounded wait for its bulk (TMA) row copies gave up; the outputs
+ * of the calls since the last read are then unreliable.  The kernels never
+ * hang on such a wait: they record the flag and finish.
+ */
+#define RMSN_DEVERR_PIPELINE_TIMEOUT 1u
+int rmsnorm_read_device_errors(unsigned *flags);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char *rmsnorm_status_string(int status);

@@ -23,7 +23,7 @@ import threading
 __all__ = [
     "RMSN_F32", "RMSN_F16", "RMSN_BF16", "RmsnormError", "lib", "lib_path",
     "rmsnorm_fwd", "rmsnorm_fwd_residual", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
-    "rmsnorm_status_string", "dtype_code",
+    "rmsnorm_read_device_errors", "rmsnorm_status_string", "dtype_code",
 ]
 
 RMSN_F32, RMSN_F16, RMSN_BF16 = 0, 1, 2
@@ -62,6 +62,8 @@ def lib():
             L.rmsnorm_fwd_residual.argtypes = [p, p, p, p, p, p, i64, i64, i64, f32, i32, i32, p]
             L.rmsnorm_bwd_workspace_bytes.argtypes = [i64, i64, i32, ctypes.POINTER(sz)]
             L.rmsnorm_bwd.argtypes = [p, p, p, p, p, p, p, sz, i64, i64, i64, i32, i32, p]
+            L.rmsnorm_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+            L.rmsnorm_read_device_errors.restype = i32
             L.rmsnorm_status_string.argtypes = [i32]
             L.rmsnorm_status_string.restype = ctypes.c_char_p
             for f in (L.rmsnorm_fwd, L.rmsnorm_fwd_residual, L.rmsnorm_bwd_workspace_bytes, L.rmsnorm_bwd):
@@ -133,6 +135,13 @@ def rmsnorm_fwd_residual(x, residual, weight, y, residual_out, rrms=None, eps: f
     _check("rmsnorm_fwd_residual", lib().rmsnorm_fwd_residual(
         _ptr(x), _ptr(residual), _ptr(weight), _ptr(y), _ptr(residual_out), _ptr(rrms), stride, M, H,
         float(eps), dtype_code(x.dtype), int(weight is not None), _stream(stream)))
+
+
+def rmsnorm_read_device_errors() -> int:
+    """Device error flags of the current device (synchronises; clears them)."""
+    out = ctypes.c_uint(0)
+    _check("rmsnorm_read_device_errors", lib().rmsnorm_read_device_errors(ctypes.byref(out)))
+    return out.value
 
 
 def rmsnorm_bwd_workspace_bytes(M: int, H: int, dtype) -> int:

@@ -8,9 +8,15 @@
 #include <tuple>
 
 #include "../../include/rmsnorm.h"
+#include "bulk.cuh"
 #include "launch.h"
 
 namespace rmsn {
+
+// Device-side error word: bit kErrPipelineTimeout is set when a kernel's
+// bounded wait on its bulk-copy pipeline gives up.  Read and cleared by
+// rmsnorm_read_device_errors().
+__device__ unsigned g_device_error = 0;
 
 namespace {
 
@@ -22,11 +28,17 @@ struct DevInfo {
     bool checked = false;
     int status = RMSN_OK;
     int sm_count = 0;
+    unsigned *err_word = nullptr;   // this device's copy of g_device_error
 };
 
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 std::map<std::tuple<int, const void *, int, size_t>, int> g_occ;
+std::map<std::pair<int, const void *>, size_t> g_smem_attr;
+
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline int round_up_to(int a, int b) { return ceil_div(a, b) * b; }
 
 // Kernel image for sm_103 only: check the current device once.
 int current_device(int *dev_out, int *sm_count) {
@@ -43,11 +55,19 @@ int current_device(int *dev_out, int *sm_count) {
         }
         d.status = (major == 10 && minor == 3 && sms > 0) ? RMSN_OK : RMSN_ERR_UNSUPPORTED;
         d.sm_count = sms;
+        if (d.status == RMSN_OK &&
+            cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err_word), g_device_error) != cudaSuccess)
+            return RMSN_ERR_CUDA;
         d.checked = true;
     }
     *dev_out = dev;
     *sm_count = d.sm_count;
     return d.status;
+}
+
+unsigned *device_error_word(int dev) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    return g_dev[dev].err_word;
 }
 
 bool aligned(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
@@ -130,6 +150,7 @@ int forward(const void *x, const void *residual, const void *weight, void *y, vo
         if (p != nullptr && !aligned(p, 16)) vec = false;
 
     FwdArgs a{};
+    a.err = device_error_word(dev);
     a.x = x;
     a.r = fused ? residual : nullptr;
     a.w = w;
@@ -143,11 +164,80 @@ int forward(const void *x, const void *residual, const void *weight, void *y, vo
     a.has_w = has_weight ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (H < kSmallH) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
+    RingPlan ring;
+    if (vec && plan_fwd_ring(M, (int)H, dtype, fused, sms, &ring))
+        return to_status(launch_fwd_ring(a, dtype, ring, s));
     if (fwd_row_fits((int)H, dtype, vec)) return to_status(launch_fwd_row(a, dtype, vec, sms, s));
     return to_status(launch_fwd_chunked(a, dtype, vec, sms, s));
 }
 
 }  // namespace
+
+cudaError_t allow_dynamic_smem(const void *func, size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const auto key = std::make_pair(dev, func);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_smem_attr.find(key);
+        if (it != g_smem_attr.end() && it->second >= bytes) return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_mu);
+    size_t &v = g_smem_attr[key];
+    if (bytes > v) v = bytes;
+    return cudaSuccess;
+}
+
+namespace {
+
+void finish_ring(RingPlan *p, int nv, int threads, int64_t row_bytes, int streams, int stages, int max_cps) {
+    const uint32_t pitch = (uint32_t)round_up_to((int)row_bytes, 128);
+    p->nv = nv;
+    p->threads = threads;
+    p->grid = 0;
+    p->max_ctas_per_sm = max_cps;
+    p->shape.stages = stages;
+    p->shape.row_bytes = (uint32_t)row_bytes;
+    p->shape.row_pitch = pitch;
+    p->smem_bytes = kRingHeaderBytes + (size_t)stages * streams * pitch;
+}
+
+}  // namespace
+
+// Forward: rows of at least 8 KB.  Two 16-byte groups per thread (four above
+// 1024 groups), two stages, two CTAs per SM: measured best at H = 4096-8192
+// (deeper rings or more CTAs per SM put more rows in flight and lose DRAM
+// efficiency); shorter rows run faster on the register kernel.
+bool fwd_ring_geometry(int H, int dtype, bool resid, RingPlan *p) {
+    const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
+    if (row_bytes % 16 != 0 || row_bytes < 8192) return false;
+    const int nvec = (int)(row_bytes / 16);
+    const int nv = nvec <= 1024 ? 2 : 4;
+    const int threads = round_up_to(ceil_div(nvec, nv), 32);
+    if (threads > 512) return false;
+    finish_ring(p, nv, threads, row_bytes, resid ? 2 : 1, 2, 2);
+    return true;
+}
+
+// Backward: about nvec/4 threads (128..512), two stages, as many CTAs per SM
+// as fit: measured best at H = 4096-8192.
+bool bwd_ring_geometry(int H, int dtype, RingPlan *p) {
+    const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
+    if (row_bytes % 16 != 0 || row_bytes < 2048) return false;
+    const int nvec = (int)(row_bytes / 16);
+    int threads = round_up_to(ceil_div(nvec, 4), 32);
+    if (threads < 128) threads = 128;
+    if (threads > 512) threads = 512;
+    const int nv = ceil_div(nvec, threads);
+    if (nv > 4) return false;
+    const size_t smem = kRingHeaderBytes + 2 * 2 * (size_t)round_up_to((int)row_bytes, 128);
+    if (smem > 200 * 1024) return false;
+    finish_ring(p, nv, threads, row_bytes, 2, 2, 0);
+    return true;
+}
 
 int occupancy(const void *func, int threads, size_t smem) {
     int dev = 0;
@@ -254,6 +344,7 @@ RMSN_API int rmsnorm_bwd(const void *dy, const void *x, const void *weight, cons
             if (k != 4 + o && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
 
     BwdArgs a{};
+    a.err = device_error_word(dev);
     a.dy = dy;
     a.x = x;
     a.w = w;
@@ -265,6 +356,21 @@ RMSN_API int rmsnorm_bwd(const void *dy, const void *x, const void *weight, cons
     a.H = (int)H;
     a.has_w = has_weight ? 1 : 0;
     return to_status(launch_bwd(a, plan, dtype, vec, dw, static_cast<cudaStream_t>(stream)));
+}
+
+RMSN_API int rmsnorm_read_device_errors(unsigned *flags) {
+    if (flags == nullptr) return RMSN_ERR_INVALID;
+    *flags = 0;
+    int dev = 0, sms = 0;
+    int st = current_device(&dev, &sms);
+    if (st) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RMSN_ERR_CUDA;
+    unsigned *word = device_error_word(dev);
+    unsigned zero = 0;
+    if (cudaMemcpy(flags, word, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess)
+        return RMSN_ERR_CUDA;
+    return RMSN_OK;
 }
 
 RMSN_API const char *rmsnorm_status_string(int status) {

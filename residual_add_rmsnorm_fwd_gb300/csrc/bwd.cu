@@ -60,12 +60,15 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
+                float d[VEC], xv[VEC], wv[VEC];
+                unpack(gp[i], d);
+                unpack(xp[i], xv);
+                unpack(wp[i], wv);
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) {
-                    const float d = to_f32(gp[i].v[j]);
-                    const float xh = to_f32(xp[i].v[j]) * rr;
-                    dot += (d * to_f32(wp[i].v[j])) * xh;
-                    acc[i][j] += d * xh;
+                    const float xh = xv[j] * rr;
+                    dot += (d[j] * wv[j]) * xh;
+                    acc[i][j] += d[j] * xh;
                 }
             }
         }
@@ -75,14 +78,13 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
-                P o;
+                float d[VEC], xv[VEC], wv[VEC];
+                unpack(gp[i], d);
+                unpack(xp[i], xv);
+                unpack(wp[i], wv);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const float g = to_f32(gp[i].v[j]) * to_f32(wp[i].v[j]);
-                    const float xh = to_f32(xp[i].v[j]) * rr;
-                    o.v[j] = from_f32<T>(rr * (g - xh * c_row));
-                }
-                st_global<T, VEC>(dx + base + (int64_t)c * VEC, o);
+                for (int j = 0; j < VEC; ++j) d[j] = rr * (d[j] * wv[j] - (xv[j] * rr) * c_row);
+                st_global<T, VEC>(dx + base + (int64_t)c * VEC, pack<T, VEC>(d));
             }
         }
     }
@@ -146,9 +148,12 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * blockDim.x + threadIdx.x;
                 if (c < nvec) {
+                    float d[VEC], xv[VEC], wv[VEC];
+                    unpack(gp[u], d);
+                    unpack(xp[u], xv);
+                    unpack(wp[u], wv);
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        dot += (to_f32(gp[u].v[j]) * to_f32(wp[u].v[j])) * (to_f32(xp[u].v[j]) * rr);
+                    for (int j = 0; j < VEC; ++j) dot += (d[j] * wv[j]) * (xv[j] * rr);
                 }
             }
         }
@@ -169,18 +174,20 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * blockDim.x + threadIdx.x;
                 if (c < nvec) {
-                    P o;
+                    float d[VEC], xv[VEC], wv[VEC], o[VEC];
+                    unpack(gp[u], d);
+                    unpack(xp[u], xv);
+                    unpack(wp[u], wv);
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
-                        const float d = to_f32(gp[u].v[j]);
-                        const float xh = to_f32(xp[u].v[j]) * rr;
-                        o.v[j] = from_f32<T>(rr * (d * to_f32(wp[u].v[j]) - xh * c_row));
+                        const float xh = xv[j] * rr;
+                        o[j] = rr * (d[j] * wv[j] - xh * c_row);
                         if (prow != nullptr) {
                             float *p = prow + (int64_t)c * VEC + j;
-                            *p = first ? d * xh : *p + d * xh;
+                            *p = first ? d[j] * xh : *p + d[j] * xh;
                         }
                     }
-                    st_global<T, VEC>(dx + base + (int64_t)c * VEC, o);
+                    st_global<T, VEC>(dx + base + (int64_t)c * VEC, pack<T, VEC>(o));
                 }
             }
         }
@@ -188,17 +195,23 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
 }
 
 // dweight_h = sum_{b = 0}^{G-1} partial[b][h].  A CTA covers 32 columns with
-// 8 warps; warp k sums the contiguous slice of partial rows
-// [k*G/8, (k+1)*G/8) in ascending order, then the 8 slice sums are added in
-// ascending k.  Fixed order, so the result is reproducible.
-__global__ void __launch_bounds__(256) dweight_reduce_kernel(const float *__restrict__ partial, int G, int H,
-                                                             float *__restrict__ dweight) {
-    __shared__ float part[8][33];
+// kReduceSlices warps; warp k sums the contiguous slice of partial rows
+// [k*G/S, (k+1)*G/S) in ascending order, then the slice sums are added in
+// ascending k.  The order depends only on G, so the result is reproducible.
+// Launched as a programmatic dependent of the backward kernel: its CTAs may
+// start early and wait here for that grid's completion and memory flush.
+constexpr int kReduceSlices = 16;
+
+__global__ void __launch_bounds__(32 * kReduceSlices)
+    dweight_reduce_kernel(const float *__restrict__ partial, int G, int H, float *__restrict__ dweight) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ float part[kReduceSlices][33];
     const int col = threadIdx.x & 31, k = threadIdx.x >> 5;
     const int h = blockIdx.x * 32 + col;
     float s = 0.0f;
     if (h < H) {
-        const int g0 = (int)((int64_t)G * k / 8), g1 = (int)((int64_t)G * (k + 1) / 8);
+        const int g0 = (int)((int64_t)G * k / kReduceSlices), g1 = (int)((int64_t)G * (k + 1) / kReduceSlices);
+#pragma unroll 4
         for (int g = g0; g < g1; ++g) s += __ldg(partial + (int64_t)g * H + h);
     }
     part[k][col] = s;
@@ -206,7 +219,7 @@ __global__ void __launch_bounds__(256) dweight_reduce_kernel(const float *__rest
     if (k == 0 && h < H) {
         float t = 0.0f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) t += part[q][col];
+        for (int q = 0; q < kReduceSlices; ++q) t += part[q][col];
         dweight[h] = t;
     }
 }
@@ -266,11 +279,12 @@ const void *chunked_kernel_for(bool vec) {
 }
 
 const void *kernel_for(const BwdPlan &p, int dtype, bool vec) {
+    if (p.kind == kBwdRing) return bwd_ring_kernel_for(dtype, p.nv);
+    const bool row = p.kind == kBwdRow;
     switch (dtype) {
-    case kF32: return p.row ? row_kernel_for<float>(vec, p.nv) : chunked_kernel_for<float>(vec);
-    case kF16: return p.row ? row_kernel_for<__half>(vec, p.nv) : chunked_kernel_for<__half>(vec);
-    case kBF16:
-        return p.row ? row_kernel_for<__nv_bfloat16>(vec, p.nv) : chunked_kernel_for<__nv_bfloat16>(vec);
+    case kF32: return row ? row_kernel_for<float>(vec, p.nv) : chunked_kernel_for<float>(vec);
+    case kF16: return row ? row_kernel_for<__half>(vec, p.nv) : chunked_kernel_for<__half>(vec);
+    case kBF16: return row ? row_kernel_for<__nv_bfloat16>(vec, p.nv) : chunked_kernel_for<__nv_bfloat16>(vec);
     }
     return nullptr;
 }
@@ -279,14 +293,25 @@ const void *kernel_for(const BwdPlan &p, int dtype, bool vec) {
 
 BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, int sm_count) {
     BwdPlan p{};
-    const int nvec = vec ? H / vec_elems(dtype) : H;
-    p.row = pick_row(nvec, vec, p.threads, p.nv);
-    if (!p.row) {
-        p.threads = kChunkThreads;
-        p.nv = 0;
+    RingPlan rp{};
+    if (vec && bwd_ring_geometry(H, dtype, &rp)) {
+        p.kind = kBwdRing;
+        p.threads = rp.threads;
+        p.nv = rp.nv;
+        p.smem_bytes = rp.smem_bytes;
+        p.ring = rp.shape;
+    } else {
+        const int nvec = vec ? H / vec_elems(dtype) : H;
+        p.kind = pick_row(nvec, vec, p.threads, p.nv) ? kBwdRow : kBwdChunked;
+        if (p.kind == kBwdChunked) {
+            p.threads = kChunkThreads;
+            p.nv = 0;
+        }
     }
     const void *k = kernel_for(p, dtype, vec);
-    const int occ = k ? occupancy(k, p.threads, 0) : 0;
+    int occ = 0;
+    if (k != nullptr && allow_dynamic_smem(k, p.smem_bytes) == cudaSuccess)
+        occ = occupancy(k, p.threads, p.smem_bytes);
     const int64_t cap = (int64_t)(occ > 0 ? occ : 1) * sm_count;
     p.grid = (int)(M < cap ? (M > 0 ? M : 1) : cap);
     return p;
@@ -298,13 +323,25 @@ cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, 
                        cudaStream_t st) {
     const void *k = kernel_for(p, dtype, vec);
     if (k == nullptr) return cudaErrorInvalidValue;
+    cudaError_t e = allow_dynamic_smem(k, p.smem_bytes);
+    if (e != cudaSuccess) return e;
     BwdArgs args = a;
-    void *params[] = {&args};
-    cudaError_t e = cudaLaunchKernel(k, dim3((unsigned)p.grid), dim3((unsigned)p.threads), params, 0, st);
+    RingShape shape = p.ring;
+    void *params[] = {&args, &shape};
+    e = cudaLaunchKernel(k, dim3((unsigned)p.grid), dim3((unsigned)p.threads), params, p.smem_bytes, st);
     if (e != cudaSuccess) return e;
     if (dweight != nullptr && a.partial != nullptr) {
-        dweight_reduce_kernel<<<(unsigned)((a.H + 31) / 32), 256, 0, st>>>(a.partial, p.grid, a.H, dweight);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)((a.H + 31) / 32));
+        cfg.blockDim = dim3(32 * kReduceSlices);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, dweight_reduce_kernel, (const float *)a.partial, p.grid, a.H, dweight);
     }
     return e;
 }

@@ -1,0 +1,167 @@
+// bwd_ring.cu -- RMSNorm backward with the dy and x rows staged in shared
+// memory by bulk copies (TMA), for 16-byte aligned rows.
+//
+// Same arithmetic as the register-resident backward kernel (bwd.cu):
+//     dot  = sum_h (dy_h * w_h) * (x_h * rrms)          (CTA reduction)
+//     dx_h = rrms * (dy_h * w_h - (x_h * rrms) * dot / H)
+//     partial[b][h] += dy_h * (x_h * rrms)               (CTA b's rows)
+// but the rows arrive through a ring of NST shared-memory stages kept full by
+// one thread's cp.async.bulk copies (mbarrier byte counts), so the next rows
+// stream in from HBM while the current one is reduced and written.  The
+// thread-to-column map is fixed, so each thread keeps its dweight partials
+// for its columns in registers across all rows of its CTA.
+#include "bulk.cuh"
+#include "launch.h"
+
+namespace rmsn {
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) {
+    constexpr int VEC = Vec16<T>::n;
+    using P = Pack<T, VEC>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[64];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    unsigned char *stages = smem + kRingHeaderBytes;
+
+    const T *__restrict__ dy = static_cast<const T *>(a.dy);
+    const T *__restrict__ x = static_cast<const T *>(a.x);
+    const T *__restrict__ w = static_cast<const T *>(a.w);
+    T *__restrict__ dx = static_cast<T *>(a.dx);
+    const int nvec = a.H / VEC;
+    const float hf = (float)a.H;
+    const int nst = rs.stages;
+    const int64_t G = gridDim.x;
+    const int64_t nrows = (a.M - 1 - blockIdx.x) / G + 1;  // the grid never exceeds M
+
+    auto stage = [&](int s, int j) { return stages + (size_t)(s * 2 + j) * rs.row_pitch; };
+    auto issue = [&](int64_t k) {
+        const int s = (int)(k % nst);
+        const int64_t base = (blockIdx.x + k * G) * a.stride;
+        mbar_arrive_expect_tx(&full[s], 2 * rs.row_bytes);
+        bulk_g2s(stage(s, 0), dy + base, rs.row_bytes, &full[s]);
+        bulk_g2s(stage(s, 1), x + base, rs.row_bytes, &full[s]);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nst; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int64_t k = 0; k < nst && k < nrows; ++k) issue(k);
+
+    P wp[NV];
+    float acc[NV][VEC];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        wp[i] = (a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc[i][j] = 0.0f;
+    }
+
+    int bank = 0;
+    bool gave_up = false;
+    float rr_next = __ldg(a.rrms + blockIdx.x);
+    for (int64_t k = 0; k < nrows; ++k) {
+        const int s = (int)(k % nst);
+        const int64_t base = (blockIdx.x + k * G) * a.stride;
+        const float rr = rr_next;
+        if (k + 1 < nrows) rr_next = __ldg(a.rrms + blockIdx.x + (k + 1) * G);
+        if (!mbar_wait_bounded(&full[s], (uint32_t)((k / nst) & 1), a.err)) gave_up = true;
+
+        P gp[NV], xp[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+                gp[i] = *reinterpret_cast<const P *>(stage(s, 0) + (size_t)c * 16);
+                xp[i] = *reinterpret_cast<const P *>(stage(s, 1) + (size_t)c * 16);
+            }
+        }
+        float dot = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+                float d[VEC], xv[VEC], wv[VEC];
+                unpack(gp[i], d);
+                unpack(xp[i], xv);
+                unpack(wp[i], wv);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const float xh = xv[j] * rr;
+                    dot += (d[j] * wv[j]) * xh;
+                    acc[i][j] += d[j] * xh;
+                }
+            }
+        }
+        // the reduction barrier also frees stage s for the row nst ahead
+        const float c_row = block_sum(dot, red, bank) / hf;
+        bank ^= 1;
+        if (threadIdx.x == 0 && k + nst < nrows) {
+            fence_proxy_async_smem();
+            issue(k + nst);
+        }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+                float d[VEC], xv[VEC], wv[VEC];
+                unpack(gp[i], d);
+                unpack(xp[i], xv);
+                unpack(wp[i], wv);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) d[j] = rr * (d[j] * wv[j] - (xv[j] * rr) * c_row);
+                st_global<T, VEC>(dx + base + (int64_t)c * VEC, pack<T, VEC>(d));
+            }
+        }
+    }
+
+    if (a.partial != nullptr) {
+        float *prow = a.partial + (int64_t)blockIdx.x * a.H;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < nvec) {
+#pragma unroll
+                for (int j = 0; j < VEC; j += 4)
+                    *reinterpret_cast<float4 *>(prow + (int64_t)c * VEC + j) =
+                        make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
+            }
+        }
+    }
+    if (gave_up && threadIdx.x == 0) {
+        for (int s = 0; s < nst && s < nrows; ++s) {
+            const int64_t uses = (nrows - 1 - s) / nst + 1;
+            mbar_wait_bounded(&full[s], (uint32_t)((uses - 1) & 1), nullptr);
+        }
+    }
+}
+
+namespace {
+
+template <typename T>
+const void *kernel_nv(int nv) {
+    switch (nv) {
+    case 1: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 1>);
+    case 2: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 2>);
+    case 3: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 3>);
+    case 4: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 4>);
+    }
+    return nullptr;
+}
+
+}  // namespace
+
+const void *bwd_ring_kernel_for(int dtype, int nv) {
+    switch (dtype) {
+    case kF32: return kernel_nv<float>(nv);
+    case kF16: return kernel_nv<__half>(nv);
+    case kBF16: return kernel_nv<__nv_bfloat16>(nv);
+    }
+    return nullptr;
+}
+
+}  // namespace rmsn

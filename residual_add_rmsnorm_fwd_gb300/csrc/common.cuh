@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace rmsn {
 
 // ---------------------------------------------------------------------------
@@ -25,6 +27,7 @@ struct FwdArgs {
     int H;
     float eps;
     int has_w;
+    unsigned *err;        // device error word (bounded pipeline waits report here)
 };
 
 struct BwdArgs {
@@ -38,7 +41,20 @@ struct BwdArgs {
     int64_t M;
     int H;
     int has_w;
+    unsigned *err;
 };
+
+// Geometry of a shared-memory row ring (bulk-copy kernels).
+struct RingShape {
+    int stages;           // rows in flight per CTA
+    uint32_t row_bytes;   // H * sizeof(T), a multiple of 16
+    uint32_t row_pitch;   // row_bytes rounded up to 128
+};
+
+// Bytes reserved at the start of a ring kernel's dynamic shared memory for
+// its mbarriers (one 8-byte barrier per stage, at most 16 stages).
+constexpr int kRingHeaderBytes = 128;
+constexpr int kRingMaxStages = 16;
 
 // ---------------------------------------------------------------------------
 // Storage types
@@ -112,6 +128,54 @@ __device__ __forceinline__ void st_global(T *p, const Pack<T, N> &v) {
         static_assert(N == 1, "scalar path stores one element");
         p[0] = v.v[0];
     }
+}
+
+// Whole-pack conversions.  16-byte packs of 2-byte types are handled as four
+// 32-bit words holding two elements each, so a pack stays in 4 registers:
+// bfloat16 is the upper half of a binary32, so widening is a shift or a mask;
+// binary16 widens with the half2 intrinsic; narrowing rounds two values at a
+// time to nearest even with the paired conversion intrinsics.
+template <typename T, int N>
+__device__ __forceinline__ void unpack(const Pack<T, N> &p, float (&f)[N]) {
+    if constexpr (sizeof(T) == 2 && N % 2 == 0) {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(&p);
+#pragma unroll
+        for (int q = 0; q < N / 2; ++q) {
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                f[2 * q] = __uint_as_float(w[q] << 16);
+                f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+            } else {
+                const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[q]));
+                f[2 * q] = t.x;
+                f[2 * q + 1] = t.y;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) f[j] = to_f32(p.v[j]);
+    }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ Pack<T, N> pack(const float (&f)[N]) {
+    Pack<T, N> p;
+    if constexpr (sizeof(T) == 2 && N % 2 == 0) {
+        uint32_t *w = reinterpret_cast<uint32_t *>(&p);
+#pragma unroll
+        for (int q = 0; q < N / 2; ++q) {
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                const __nv_bfloat162 t = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);
+                w[q] = *reinterpret_cast<const uint32_t *>(&t);
+            } else {
+                const __half2 t = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
+                w[q] = *reinterpret_cast<const uint32_t *>(&t);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) p.v[j] = from_f32<T>(f[j]);
+    }
+    return p;
 }
 
 template <typename T, int N>

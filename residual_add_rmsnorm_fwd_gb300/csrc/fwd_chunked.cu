@@ -43,12 +43,16 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * blockDim.x + threadIdx.x;
                 if (c < nvec) {
+                    float v[VEC];
+                    unpack(xp[u], v);
+                    if constexpr (RESID) {
+                        float rv[VEC];
+                        unpack(rp[u], rv);
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        float s = to_f32(xp[u].v[j]);
-                        if constexpr (RESID) s += to_f32(rp[u].v[j]);
-                        ss += s * s;
+                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
                     }
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) ss += v[j] * v[j];
                 }
             }
         }
@@ -72,18 +76,19 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * blockDim.x + threadIdx.x;
                 if (c < nvec) {
-                    P yo, so;
+                    float v[VEC], wv[VEC];
+                    unpack(xp[u], v);
+                    if constexpr (RESID) {
+                        float rv[VEC];
+                        unpack(rp[u], rv);
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        float s = to_f32(xp[u].v[j]);
-                        if constexpr (RESID) {
-                            s += to_f32(rp[u].v[j]);
-                            so.v[j] = from_f32<T>(s);
-                        }
-                        yo.v[j] = from_f32<T>((s * rrms) * to_f32(wp[u].v[j]));
+                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                        st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
                     }
-                    if constexpr (RESID) st_global<T, VEC>(s_out + base + (int64_t)c * VEC, so);
-                    st_global<T, VEC>(y + base + (int64_t)c * VEC, yo);
+                    unpack(wp[u], wv);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
+                    st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
                 }
             }
         }

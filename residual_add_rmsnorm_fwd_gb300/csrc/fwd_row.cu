@@ -52,17 +52,17 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
-                P so;
+                float v[VEC];
+                unpack(xp[i], v);
+                if constexpr (RESID) {
+                    float rv[VEC];
+                    unpack(rp[i], rv);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    float s = to_f32(xp[i].v[j]);
-                    if constexpr (RESID) {
-                        s += to_f32(rp[i].v[j]);
-                        so.v[j] = from_f32<T>(s);
-                    }
-                    ss += s * s;
+                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                    st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
                 }
-                if constexpr (RESID) st_global<T, VEC>(s_out + base + (int64_t)c * VEC, so);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) ss += v[j] * v[j];
             }
         }
         const float total = block_sum(ss, red, bank);
@@ -75,14 +75,18 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
-                P yo;
+                float v[VEC], wv[VEC];
+                unpack(xp[i], v);
+                if constexpr (RESID) {
+                    float rv[VEC];
+                    unpack(rp[i], rv);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    float s = to_f32(xp[i].v[j]);
-                    if constexpr (RESID) s += to_f32(rp[i].v[j]);
-                    yo.v[j] = from_f32<T>((s * rrms) * to_f32(wp[i].v[j]));
+                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
                 }
-                st_global<T, VEC>(y + base + (int64_t)c * VEC, yo);
+                unpack(wp[i], wv);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
+                st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
             }
         }
     }
@@ -96,16 +100,20 @@ constexpr int kScalarNV[] = {1, 2, 4, 8, 16};
 
 inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
-// Smallest NV (from the instantiated set) whose thread count fits a CTA.
+// Column groups per thread: the smallest CTA of at most 128, else 256, else
+// 512 threads that covers the row (measured: 128 threads x 2 groups is best
+// at H = 2048 bf16; larger aligned rows go to the bulk-copy ring kernel).
 bool pick(int nvec, bool vec, int &threads, int &nv) {
     const int *set = vec ? kVecNV : kScalarNV;
     const int n = vec ? 4 : 5;
-    for (int k = 0; k < n; ++k) {
-        const int t = round_up((nvec + set[k] - 1) / set[k], 32);
-        if (t <= kMaxThreads) {
-            threads = t;
-            nv = set[k];
-            return true;
+    for (int cap : {128, 256, kMaxThreads}) {
+        for (int k = 0; k < n; ++k) {
+            const int t = round_up((nvec + set[k] - 1) / set[k], 32);
+            if (t <= cap) {
+                threads = t;
+                nv = set[k];
+                return true;
+            }
         }
     }
     return false;

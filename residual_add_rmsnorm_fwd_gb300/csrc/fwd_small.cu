@@ -56,17 +56,17 @@ __global__ void __launch_bounds__(256) fwd_small_kernel(FwdArgs a) {
         for (int k = 0; k < NPL; ++k) {
             const int c = li + k * LANES;
             if (live && c < nvec) {
-                P so;
+                float v[VEC];
+                unpack(xp[k], v);
+                if constexpr (RESID) {
+                    float rv[VEC];
+                    unpack(rp[k], rv);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    float s = to_f32(xp[k].v[j]);
-                    if constexpr (RESID) {
-                        s += to_f32(rp[k].v[j]);
-                        so.v[j] = from_f32<T>(s);
-                    }
-                    ss += s * s;
+                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                    st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
                 }
-                if constexpr (RESID) st_global<T, VEC>(s_out + base + (int64_t)c * VEC, so);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) ss += v[j] * v[j];
             }
         }
         const float total = group_sum<LANES>(ss);
@@ -76,14 +76,18 @@ __global__ void __launch_bounds__(256) fwd_small_kernel(FwdArgs a) {
         for (int k = 0; k < NPL; ++k) {
             const int c = li + k * LANES;
             if (live && c < nvec) {
-                P yo;
+                float v[VEC], wv[VEC];
+                unpack(xp[k], v);
+                if constexpr (RESID) {
+                    float rv[VEC];
+                    unpack(rp[k], rv);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    float s = to_f32(xp[k].v[j]);
-                    if constexpr (RESID) s += to_f32(rp[k].v[j]);
-                    yo.v[j] = from_f32<T>((s * rrms) * to_f32(wp[k].v[j]));
+                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
                 }
-                st_global<T, VEC>(y + base + (int64_t)c * VEC, yo);
+                unpack(wp[k], wv);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
+                st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
             }
         }
     }

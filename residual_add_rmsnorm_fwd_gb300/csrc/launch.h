@@ -19,6 +19,29 @@ inline int vec_elems(int dtype) { return 16 / elem_bytes(dtype); }
 // that fit on one SM of the current device (cached per device).
 int occupancy(const void *func, int threads, size_t smem);
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` (once per device).
+cudaError_t allow_dynamic_smem(const void *func, size_t bytes);
+
+// A ring kernel launch: NV 16-byte column groups per thread, `threads` per
+// CTA, `grid` persistent CTAs, the shared-memory ring geometry.
+struct RingPlan {
+    int nv;
+    int threads;
+    int grid;
+    int max_ctas_per_sm;   // 0 = as many as fit
+    size_t smem_bytes;
+    RingShape shape;
+};
+
+// Ring shapes measured best on GB300 (see the kernel files): false when the
+// row is too short to profit from the ring or too long for it.
+bool fwd_ring_geometry(int H, int dtype, bool resid, RingPlan *p);
+bool bwd_ring_geometry(int H, int dtype, RingPlan *p);
+
+// Forward with rows staged by bulk copies (16-byte aligned rows only).
+bool plan_fwd_ring(int64_t M, int H, int dtype, bool resid, int sm_count, RingPlan *out);
+cudaError_t launch_fwd_ring(const FwdArgs &a, int dtype, const RingPlan &p, cudaStream_t st);
+
 // Small H (below 256): a warp, or an aligned group of 1..32 lanes, per row.
 cudaError_t launch_fwd_small(const FwdArgs &a, int dtype, bool vec, int sm_count, cudaStream_t st);
 
@@ -31,12 +54,16 @@ cudaError_t launch_fwd_chunked(const FwdArgs &a, int dtype, bool vec, int sm_cou
 
 // Backward: dx per row plus per-CTA dweight partials, then the fixed-order
 // column reduction of the partials.
+enum BwdKind { kBwdRow = 0, kBwdChunked = 1, kBwdRing = 2 };
 struct BwdPlan {
-    bool row;        // register-resident row kernel (else the chunked kernel)
+    int kind;        // BwdKind
     int threads;
-    int nv;          // vectors per thread (row kernel)
+    int nv;          // 16-byte groups (or elements) per thread (row and ring kernels)
     int grid;        // persistent CTAs = rows of the partial buffer
+    size_t smem_bytes;
+    RingShape ring;
 };
+const void *bwd_ring_kernel_for(int dtype, int nv);
 BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, int sm_count);
 size_t bwd_partial_bytes(const BwdPlan &p, int H);
 cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, float *dweight,
