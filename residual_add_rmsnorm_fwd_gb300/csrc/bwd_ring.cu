@@ -9,7 +9,10 @@
 // one thread's cp.async.bulk copies (mbarrier byte counts), so the next rows
 // stream in from HBM while the current one is reduced and written.  The
 // thread-to-column map is fixed, so each thread keeps its dweight partials
-// for its columns in registers across all rows of its CTA.
+// for its columns in registers across all rows of its CTA.  A thread keeps
+// its packed dy and x groups in registers across the reduction barrier, so
+// the stage is refilled right after that barrier (measured faster than
+// re-reading the stage after the barrier and refilling one row later).
 #include "bulk.cuh"
 #include "launch.h"
 
@@ -18,6 +21,7 @@ namespace rmsn {
 template <typename T, int NV>
 __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) {
     constexpr int VEC = Vec16<T>::n;
+    constexpr int PR = Pairs16<T>::n;
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
@@ -52,13 +56,13 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
         for (int64_t k = 0; k < nst && k < nrows; ++k) issue(k);
 
     P wp[NV];
-    float acc[NV][VEC];
+    f32x2 acc[NV][PR];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int c = threadIdx.x + i * blockDim.x;
         wp[i] = (a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) acc[i][j] = 0.0f;
+        for (int q = 0; q < PR; ++q) acc[i][q] = f2_make(0.0f, 0.0f);
     }
 
     int bank = 0;
@@ -69,52 +73,49 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
         const int64_t base = (blockIdx.x + k * G) * a.stride;
         const float rr = rr_next;
         if (k + 1 < nrows) rr_next = __ldg(a.rrms + blockIdx.x + (k + 1) * G);
+        const f32x2 rr2 = f2_make(rr, rr);
         if (!mbar_wait_bounded(&full[s], (uint32_t)((k / nst) & 1), a.err)) gave_up = true;
 
         P gp[NV], xp[NV];
+        f32x2 dot2 = f2_make(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
                 gp[i] = *reinterpret_cast<const P *>(stage(s, 0) + (size_t)c * 16);
                 xp[i] = *reinterpret_cast<const P *>(stage(s, 1) + (size_t)c * 16);
-            }
-        }
-        float dot = 0.0f;
+                f32x2 d[PR], xv[PR], wv[PR];
+                widen16<T>(gp[i], d);
+                widen16<T>(xp[i], xv);
+                widen16<T>(wp[i], wv);
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int c = threadIdx.x + i * blockDim.x;
-            if (c < nvec) {
-                float d[VEC], xv[VEC], wv[VEC];
-                unpack(gp[i], d);
-                unpack(xp[i], xv);
-                unpack(wp[i], wv);
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const float xh = xv[j] * rr;
-                    dot += (d[j] * wv[j]) * xh;
-                    acc[i][j] += d[j] * xh;
+                for (int q = 0; q < PR; ++q) {
+                    const f32x2 xh = f2_mul(xv[q], rr2);
+                    dot2 = f2_fma(f2_mul(d[q], wv[q]), xh, dot2);
+                    acc[i][q] = f2_fma(d[q], xh, acc[i][q]);
                 }
             }
         }
         // the reduction barrier also frees stage s for the row nst ahead
-        const float c_row = block_sum(dot, red, bank) / hf;
+        const float c_row = block_sum(f2_sum(dot2), red, bank) / hf;
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
             fence_proxy_async_smem();
             issue(k + nst);
         }
+        const f32x2 nc2 = f2_make(-c_row, -c_row);
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
-                float d[VEC], xv[VEC], wv[VEC];
-                unpack(gp[i], d);
-                unpack(xp[i], xv);
-                unpack(wp[i], wv);
+                f32x2 d[PR], xv[PR], wv[PR];
+                widen16<T>(gp[i], d);
+                widen16<T>(xp[i], xv);
+                widen16<T>(wp[i], wv);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) d[j] = rr * (d[j] * wv[j] - (xv[j] * rr) * c_row);
-                st_global<T, VEC>(dx + base + (int64_t)c * VEC, pack<T, VEC>(d));
+                for (int q = 0; q < PR; ++q)   // rrms * (g - xhat * c)
+                    d[q] = f2_mul(rr2, f2_fma(f2_mul(xv[q], rr2), nc2, f2_mul(d[q], wv[q])));
+                st_global<T, VEC>(dx + base + (int64_t)c * VEC, narrow16<T>(d));
             }
         }
     }
@@ -126,9 +127,12 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
 #pragma unroll
-                for (int j = 0; j < VEC; j += 4)
-                    *reinterpret_cast<float4 *>(prow + (int64_t)c * VEC + j) =
-                        make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
+                for (int q = 0; q < PR; q += 2) {
+                    float a0, a1, a2, a3;
+                    f2_split(acc[i][q], a0, a1);
+                    f2_split(acc[i][q + 1], a2, a3);
+                    *reinterpret_cast<float4 *>(prow + (int64_t)c * VEC + 2 * q) = make_float4(a0, a1, a2, a3);
+                }
             }
         }
     }

@@ -178,6 +178,88 @@ __device__ __forceinline__ Pack<T, N> pack(const float (&f)[N]) {
     return p;
 }
 
+// ---------------------------------------------------------------------------
+// Pairs of binary32 values held in one 64-bit register pair, operated on by
+// the two-lane binary32 instructions (add/mul/fma .rn.f32x2): each lane is
+// rounded exactly as the scalar instruction would round it.
+// ---------------------------------------------------------------------------
+
+using f32x2 = unsigned long long;
+
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
+    f32x2 u;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(lo), "f"(hi));
+    return u;
+}
+__device__ __forceinline__ void f2_split(f32x2 u, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(u));
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float f2_sum(f32x2 u) {
+    float lo, hi;
+    f2_split(u, lo, hi);
+    return lo + hi;
+}
+
+// Pairs in one 16-byte vector of storage type T.
+template <typename T> struct Pairs16 { static constexpr int n = 16 / (int)sizeof(T) / 2; };
+
+// 16 bytes of storage -> binary32 pairs (exact).
+template <typename T>
+__device__ __forceinline__ void widen16(const Pack<T, 16 / sizeof(T)> &p, f32x2 (&o)[Pairs16<T>::n]) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(&p);
+    if constexpr (std::is_same<T, float>::value) {
+        o[0] = f2_make(__uint_as_float(w[0]), __uint_as_float(w[1]));
+        o[1] = f2_make(__uint_as_float(w[2]), __uint_as_float(w[3]));
+    } else if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = f2_make(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[q]));
+            o[q] = f2_make(t.x, t.y);
+        }
+    }
+}
+
+// binary32 pairs -> 16 bytes of storage, each value rounded to nearest even.
+template <typename T>
+__device__ __forceinline__ Pack<T, 16 / sizeof(T)> narrow16(const f32x2 (&v)[Pairs16<T>::n]) {
+    Pack<T, 16 / sizeof(T)> p;
+    uint32_t *w = reinterpret_cast<uint32_t *>(&p);
+#pragma unroll
+    for (int q = 0; q < Pairs16<T>::n; ++q) {
+        float lo, hi;
+        f2_split(v[q], lo, hi);
+        if constexpr (std::is_same<T, float>::value) {
+            w[2 * q] = __float_as_uint(lo);
+            w[2 * q + 1] = __float_as_uint(hi);
+        } else if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+            const __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+            w[q] = *reinterpret_cast<const uint32_t *>(&t);
+        } else {
+            const __half2 t = __floats2half2_rn(lo, hi);
+            w[q] = *reinterpret_cast<const uint32_t *>(&t);
+        }
+    }
+    return p;
+}
+
 template <typename T, int N>
 __device__ __forceinline__ Pack<T, N> fill(T v) {
     Pack<T, N> r;

@@ -8,9 +8,9 @@
 // counted by an mbarrier per stage.  So up to NST rows per CTA are in flight
 // from HBM while the CTA computes, independently of the register budget.
 // Each thread copies its NV 16-byte column groups from the stage into
-// registers, forms s = x (+ residual) in binary32, writes residual_out,
-// reduces sum(s^2) over the CTA, and writes y = (s * rrms) * w from
-// registers: the row is read from HBM once ("Skill: Write a Triton RMSNorm
+// registers, forms s = x (+ residual) in binary32 (two lanes per f32x2
+// instruction), writes residual_out, reduces sum(s^2) over the CTA, and
+// writes y = (s * rrms) * w from registers: the row is read from HBM once ("Skill: Write a Triton RMSNorm
 // Kernel", Required reasoning 3-10; Performance requirements).  The stage is
 // refilled with row k + NST as soon as the reduction barrier shows every
 // thread has copied it out.
@@ -22,7 +22,8 @@ namespace rmsn {
 template <typename T, int NV, bool RESID>
 __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) {
     constexpr int VEC = Vec16<T>::n;
-    constexpr int NS = RESID ? 2 : 1;  // streams staged per row
+    constexpr int PR = Pairs16<T>::n;   // binary32 pairs per 16-byte group
+    constexpr int NS = RESID ? 2 : 1;   // streams staged per row
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
@@ -57,11 +58,12 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     if (threadIdx.x == 0)
         for (int64_t k = 0; k < nst && k < nrows; ++k) issue(k);
 
-    P wp[NV];
+    // weight (H,), by column only, widened once per CTA; ones without weight
+    f32x2 wv[NV][PR];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int c = threadIdx.x + i * blockDim.x;
-        wp[i] = (a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+        widen16<T>((a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>()), wv[i]);
     }
 
     int bank = 0;
@@ -71,36 +73,29 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
         const int64_t base = (blockIdx.x + k * G) * a.stride;
         if (!mbar_wait_bounded(&full[s], (uint32_t)((k / nst) & 1), a.err)) gave_up = true;
 
-        P xp[NV], rp[NV];
+        // s = x (+ residual) in binary32, kept in registers for the scale step;
+        // the post-add sum is written back as the next residual stream
+        f32x2 sv[NV][PR];
+        f32x2 ss2 = f2_make(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
-                xp[i] = *reinterpret_cast<const P *>(stage(s, 0) + (size_t)c * 16);
-                if constexpr (RESID) rp[i] = *reinterpret_cast<const P *>(stage(s, 1) + (size_t)c * 16);
-            }
-        }
-        float ss = 0.0f;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int c = threadIdx.x + i * blockDim.x;
-            if (c < nvec) {
-                float v[VEC];
-                unpack(xp[i], v);
+                widen16<T>(*reinterpret_cast<const P *>(stage(s, 0) + (size_t)c * 16), sv[i]);
                 if constexpr (RESID) {
-                    float rv[VEC];
-                    unpack(rp[i], rv);
+                    f32x2 rv[PR];
+                    widen16<T>(*reinterpret_cast<const P *>(stage(s, 1) + (size_t)c * 16), rv);
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
-                    st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
+                    for (int q = 0; q < PR; ++q) sv[i][q] = f2_add(sv[i][q], rv[q]);
+                    st_global<T, VEC>(s_out + base + (int64_t)c * VEC, narrow16<T>(sv[i]));
                 }
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) ss += v[j] * v[j];
+                for (int q = 0; q < PR; ++q) ss2 = f2_fma(sv[i][q], sv[i][q], ss2);
             }
         }
         // the barrier inside the reduction also means every thread has
         // copied stage s out, so it can be refilled
-        const float total = block_sum(ss, red, bank);
+        const float total = block_sum(f2_sum(ss2), red, bank);
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
             fence_proxy_async_smem();
@@ -108,22 +103,16 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
         }
         const float rrms = rsqrtf(total / hf + a.eps);
         if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[blockIdx.x + k * G] = rrms;
+        const f32x2 rr2 = f2_make(rrms, rrms);
+        // y = (s * rrms) * w, one rounding to the storage type
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
-                float v[VEC], wv[VEC];
-                unpack(xp[i], v);
-                if constexpr (RESID) {
-                    float rv[VEC];
-                    unpack(rp[i], rv);
+                f32x2 yv[PR];
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
-                }
-                unpack(wp[i], wv);
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
-                st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
+                for (int q = 0; q < PR; ++q) yv[q] = f2_mul(f2_mul(sv[i][q], rr2), wv[i][q]);
+                st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(yv));
             }
         }
     }
