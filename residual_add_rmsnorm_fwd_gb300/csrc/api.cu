@@ -222,15 +222,17 @@ bool fwd_ring_geometry(int H, int dtype, bool resid, RingPlan *p) {
     return true;
 }
 
-// Backward: two 16-byte groups per thread up to 768 groups per row, four
-// above (H = 4096 bf16: 256 threads; 6144: 384; 8192: 256), two stages, as
-// many CTAs per SM as fit -- the backward profits from every resident warp.
-// Measured best at H = 4096-8192 on GB300.
+// Backward: bfloat16 and binary32 rows take two 16-byte groups per thread up
+// to 768 groups per row and four above (H = 4096 bf16: 256 threads; 6144:
+// 384; 8192: 256); binary16 rows take four (its widening runs on the FP32
+// pipe, and the longer per-thread chains measured faster: H = 6144 f16, 205
+// against 245 us).  Two stages, as many CTAs per SM as fit -- the backward
+// profits from every resident warp.  Measured on GB300 at H = 4096-8192.
 bool bwd_ring_geometry(int H, int dtype, RingPlan *p) {
     const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
     if (row_bytes % 16 != 0 || row_bytes < 2048) return false;
     const int nvec = (int)(row_bytes / 16);
-    const int nv = nvec <= 768 ? 2 : 4;
+    const int nv = (dtype != kF16 && nvec <= 768) ? 2 : 4;
     const int threads = round_up_to(ceil_div(nvec, nv), 32);
     if (threads > 512) return false;
     const int stages = 2;

@@ -130,54 +130,6 @@ __device__ __forceinline__ void st_global(T *p, const Pack<T, N> &v) {
     }
 }
 
-// Whole-pack conversions.  16-byte packs of 2-byte types are handled as four
-// 32-bit words holding two elements each, so a pack stays in 4 registers:
-// bfloat16 is the upper half of a binary32, so widening is a shift or a mask;
-// binary16 widens with the half2 intrinsic; narrowing rounds two values at a
-// time to nearest even with the paired conversion intrinsics.
-template <typename T, int N>
-__device__ __forceinline__ void unpack(const Pack<T, N> &p, float (&f)[N]) {
-    if constexpr (sizeof(T) == 2 && N % 2 == 0) {
-        const uint32_t *w = reinterpret_cast<const uint32_t *>(&p);
-#pragma unroll
-        for (int q = 0; q < N / 2; ++q) {
-            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-                f[2 * q] = __uint_as_float(w[q] << 16);
-                f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
-            } else {
-                const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[q]));
-                f[2 * q] = t.x;
-                f[2 * q + 1] = t.y;
-            }
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < N; ++j) f[j] = to_f32(p.v[j]);
-    }
-}
-
-template <typename T, int N>
-__device__ __forceinline__ Pack<T, N> pack(const float (&f)[N]) {
-    Pack<T, N> p;
-    if constexpr (sizeof(T) == 2 && N % 2 == 0) {
-        uint32_t *w = reinterpret_cast<uint32_t *>(&p);
-#pragma unroll
-        for (int q = 0; q < N / 2; ++q) {
-            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-                const __nv_bfloat162 t = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);
-                w[q] = *reinterpret_cast<const uint32_t *>(&t);
-            } else {
-                const __half2 t = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
-                w[q] = *reinterpret_cast<const uint32_t *>(&t);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < N; ++j) p.v[j] = from_f32<T>(f[j]);
-    }
-    return p;
-}
-
 // ---------------------------------------------------------------------------
 // Pairs of binary32 values held in one 64-bit register pair, operated on by
 // the two-lane binary32 instructions (add/mul/fma .rn.f32x2): each lane is
@@ -215,6 +167,21 @@ __device__ __forceinline__ float f2_sum(f32x2 u) {
     return lo + hi;
 }
 
+// Two IEEE binary16 values (one 32-bit word, low half first) -> binary32
+// pair, exactly, with the mixed-precision add (binary16 operand widened
+// inside a binary32 add) on the FP32 pipe rather than the conversion pipe:
+// h + (-0) = h for every h, including -0, infinities and NaN.
+__device__ __forceinline__ f32x2 widen_f16x2(uint32_t w) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.f16 %0, l, 0f80000000;\n\t"
+        "add.rn.f32.f16 %1, h, 0f80000000;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+    return f2_make(lo, hi);
+}
+
 // Pairs in one 16-byte vector of storage type T.
 template <typename T> struct Pairs16 { static constexpr int n = 16 / (int)sizeof(T) / 2; };
 
@@ -230,10 +197,7 @@ __device__ __forceinline__ void widen16(const Pack<T, 16 / sizeof(T)> &p, f32x2 
         for (int q = 0; q < 4; ++q) o[q] = f2_make(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
     } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[q]));
-            o[q] = f2_make(t.x, t.y);
-        }
+        for (int q = 0; q < 4; ++q) o[q] = widen_f16x2(w[q]);
     }
 }
 
@@ -256,6 +220,52 @@ __device__ __forceinline__ Pack<T, 16 / sizeof(T)> narrow16(const f32x2 (&v)[Pai
             const __half2 t = __floats2half2_rn(lo, hi);
             w[q] = *reinterpret_cast<const uint32_t *>(&t);
         }
+    }
+    return p;
+}
+
+// Whole-pack conversions.  16-byte packs of 2-byte types are handled as four
+// 32-bit words holding two elements each, so a pack stays in 4 registers:
+// bfloat16 is the upper half of a binary32, so widening is a shift or a mask;
+// binary16 widens with the half2 intrinsic; narrowing rounds two values at a
+// time to nearest even with the paired conversion intrinsics.
+template <typename T, int N>
+__device__ __forceinline__ void unpack(const Pack<T, N> &p, float (&f)[N]) {
+    if constexpr (sizeof(T) == 2 && N % 2 == 0) {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(&p);
+#pragma unroll
+        for (int q = 0; q < N / 2; ++q) {
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                f[2 * q] = __uint_as_float(w[q] << 16);
+                f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+            } else {
+                f2_split(widen_f16x2(w[q]), f[2 * q], f[2 * q + 1]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) f[j] = to_f32(p.v[j]);
+    }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ Pack<T, N> pack(const float (&f)[N]) {
+    Pack<T, N> p;
+    if constexpr (sizeof(T) == 2 && N % 2 == 0) {
+        uint32_t *w = reinterpret_cast<uint32_t *>(&p);
+#pragma unroll
+        for (int q = 0; q < N / 2; ++q) {
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                const __nv_bfloat162 t = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);
+                w[q] = *reinterpret_cast<const uint32_t *>(&t);
+            } else {
+                const __half2 t = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
+                w[q] = *reinterpret_cast<const uint32_t *>(&t);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) p.v[j] = from_f32<T>(f[j]);
     }
     return p;
 }

@@ -264,3 +264,26 @@ def test_in_place_rejected():
     with pytest.raises(rn.RmsnormError) as e:
         rn.rmsnorm_fwd(x, None, x)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("H,offset", [(4096, 0), (4096, 1), (64, 0), (8192, 0)])
+def test_storage_widening_exhaustive(dtype, H, offset):
+    """Every 16-bit pattern passes through the kernels' widening exactly:
+    with residual = -0, residual_out = x + (-0) must reproduce x bit for bit
+    (NaNs as NaNs), through the 128-bit path (offset 0) and the scalar path."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    M = 65536 // H
+    x = pats.reshape(M, H)
+    r = np.full((M, H), 0x8000, np.uint16)
+    gx = Guarded(M, H, H, dtype, offset).upload(x)
+    gr = Guarded(M, H, H, dtype, offset).upload(r)
+    gy, gs = Guarded(M, H, H, dtype, offset), Guarded(M, H, H, dtype, offset)
+    rn.rmsnorm_fwd_residual(gx.t, gr.t, None, gy.t, gs.t, None, eps=1e-5)
+    torch.cuda.synchronize()
+    got = gs.host()
+    isnan = ((x & 0x7FFF) > (0x7C00 if dtype == "f16" else 0x7F80))
+    assert np.array_equal(got[~isnan], x[~isnan])
+    nan_exp = 0x7C00 if dtype == "f16" else 0x7F80
+    assert np.all(((got[isnan] & nan_exp) == nan_exp) & ((got[isnan] & (0x3FF if dtype == "f16" else 0x7F)) != 0))
+    assert gs.untouched_outside() and gy.untouched_outside()
