@@ -135,6 +135,30 @@ int rmsnorm_bwd(const void *dy, const void *x, const void *weight, const float *
                 int dtype, int has_weight, void *stream);
 
 /*
+ * Backward for callers that cannot allocate device memory.  No counterpart
+ * on the pages: it exists for callers such as serving engines that reserve
+ * all device memory at start-up and forbid allocation afterwards, plugin
+ * interfaces that give an operator only its inputs and outputs, and hot
+ * paths where a cudaMalloc (which can synchronise the device) is not
+ * acceptable.  Same arguments, results and errors as rmsnorm_bwd without the
+ * workspace: the dweight partials live in a fixed 16 MiB array in the
+ * library's device memory (held on every GPU that loads the library until
+ * the process exits).  The call allocates nothing.
+ *   - A shape whose partials exceed 16 MiB (rmsnorm_bwd_workspace_bytes >
+ *     16 MiB) is rejected with RMSN_ERR_WORKSPACE before any launch.
+ *   - The first call on a device looks up the array's device address (one
+ *     cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the array.  Calls whose kernels may overlap on the GPU
+ *     (different streams with no ordering between them) race on it; order
+ *     them on one stream.
+ */
+int rmsnorm_bwd_noalloc(const void *dy, const void *x, const void *weight, const float *rrms,
+                        void *dx, float *dweight,
+                        int64_t row_stride, int64_t M, int64_t H,
+                        int dtype, int has_weight, void *stream);
+
+/*
  * Device-side error flags of the current device, read and cleared.
  * Synchronises the device first.  Bit 0 (RMSN_DEVERR_PIPELINE_TIMEOUT): a
  * kernel's bounded wait for its bulk (TMA) row copies gave up; the outputs

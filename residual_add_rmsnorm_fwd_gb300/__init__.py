@@ -23,7 +23,7 @@ import threading
 __all__ = [
     "RMSN_F32", "RMSN_F16", "RMSN_BF16", "RmsnormError", "lib", "lib_path",
     "rmsnorm_fwd", "rmsnorm_fwd_residual", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
-    "rmsnorm_read_device_errors", "rmsnorm_status_string", "dtype_code",
+    "rmsnorm_bwd_noalloc", "rmsnorm_read_device_errors", "rmsnorm_status_string", "dtype_code",
 ]
 
 RMSN_F32, RMSN_F16, RMSN_BF16 = 0, 1, 2
@@ -62,6 +62,8 @@ def lib():
             L.rmsnorm_fwd_residual.argtypes = [p, p, p, p, p, p, i64, i64, i64, f32, i32, i32, p]
             L.rmsnorm_bwd_workspace_bytes.argtypes = [i64, i64, i32, ctypes.POINTER(sz)]
             L.rmsnorm_bwd.argtypes = [p, p, p, p, p, p, p, sz, i64, i64, i64, i32, i32, p]
+            L.rmsnorm_bwd_noalloc.argtypes = [p, p, p, p, p, p, i64, i64, i64, i32, i32, p]
+            L.rmsnorm_bwd_noalloc.restype = i32
             L.rmsnorm_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint)]
             L.rmsnorm_read_device_errors.restype = i32
             L.rmsnorm_status_string.argtypes = [i32]
@@ -149,6 +151,15 @@ def rmsnorm_bwd_workspace_bytes(M: int, H: int, dtype) -> int:
     out = ctypes.c_size_t(0)
     _check("rmsnorm_bwd_workspace_bytes", lib().rmsnorm_bwd_workspace_bytes(M, H, code, ctypes.byref(out)))
     return out.value
+
+
+def rmsnorm_bwd_noalloc(dy, x, weight, rrms, dx, dweight=None, stream=None):
+    """rmsnorm_bwd without a workspace, for callers that must not allocate:
+    the dweight partials use the library's fixed 16 MiB device array."""
+    M, H, stride = _shared_stride([(dy, "dy"), (x, "x"), (dx, "dx")])
+    _check("rmsnorm_bwd_noalloc", lib().rmsnorm_bwd_noalloc(
+        _ptr(dy), _ptr(x), _ptr(weight), _ptr(rrms), _ptr(dx), _ptr(dweight), stride, M, H,
+        dtype_code(x.dtype), int(weight is not None), _stream(stream)))
 
 
 def rmsnorm_bwd(dy, x, weight, rrms, dx, dweight=None, workspace=None, stream=None):
