@@ -172,6 +172,8 @@ class StepWorkload:
     """Fused forward + backward on one batch (the default benchmark step)."""
     name = "fused_fwd_bwd_bf16_B8xT2048xH4096"
 
+    flush_l2 = False
+
     def __init__(self, cfg_id=2, backward=True, fused=None):
         import torch
         import residual_add_rmsnorm_fwd_gb300 as rn
@@ -228,10 +230,14 @@ class StepWorkload:
         return out
 
     def config(self):
-        return {"workload": self.name, "M": self.M, "H": self.H, "row_stride": self.S, "dtype": self.dt,
-                "B": 8, "T": 2048, "fused_residual": self.fused, "backward": self.backward,
-                "eps": self.c["eps"], "l2": "no flush: per-step working set larger than L2",
-                "algorithmic_bytes_per_step": self.bytes_per_step}
+        cfg = {"workload": self.name, "M": self.M, "H": self.H, "row_stride": self.S, "dtype": self.dt,
+               "fused_residual": self.fused, "backward": self.backward, "eps": self.c["eps"],
+               "l2": ("flushed before every step (256 MiB write); time = sum of the per-call CUDA-event "
+                      "intervals" if self.flush_l2 else "no flush: per-step working set larger than L2"),
+               "algorithmic_bytes_per_step": self.bytes_per_step}
+        if self.cfg_id == 2:
+            cfg.update(B=8, T=2048)
+        return cfg
 
     # end to end through the binding with pinned host buffers
     def e2e_setup(self):
@@ -285,6 +291,7 @@ class DitMixWorkload:
     393216 x 64, per step.  Four x/y buffer sets rotate so that consecutive
     calls never find their operands in L2."""
     name = "dit_mix_bf16_168x12288x2048_plus_heads_393216x64"
+    flush_l2 = False
 
     def __init__(self):
         import torch
@@ -362,7 +369,19 @@ class DitMixWorkload:
         return rows * self.call_bytes_w / self.M
 
 
+class SmallFwdWorkload(StepWorkload):
+    """The fp32 forward on 64 x 1024 rows: 528 KB, resident in L2 unless
+    flushed, so L2 is flushed before every step and only the kernel's own
+    interval is timed.  Latency-bound: its number is microseconds per call."""
+    name = "fwd_f32_64x1024"
+    flush_l2 = True
+
+    def __init__(self):
+        super().__init__(1, backward=False)
+
+
 WORKLOADS = {
+    "fwd_f32_small": SmallFwdWorkload,
     "dit_mix": DitMixWorkload,
     "step": lambda: StepWorkload(2, backward=True),
     "fused_fwd": lambda: StepWorkload(2, backward=False),
@@ -419,6 +438,7 @@ def run_native(args):
     torch.cuda.synchronize()
 
     K = args.steps
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if wk.flush_l2 else None
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
           for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -429,6 +449,8 @@ def run_native(args):
     t0 = time.time()
     start.record(stream)
     for k in range(K):
+        if flush is not None:
+            flush.fill_(k & 0xFF)
         for j, (_, fn, _) in enumerate(calls):
             ev[k][j][0].record(stream)
             fn()
@@ -437,8 +459,9 @@ def run_native(args):
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(world)
-    ms_total = start.elapsed_time(stop)
     per_call_ms = [[ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(K)] for j in range(len(calls))]
+    # with L2 flushes in the timed region, only the calls' own intervals count
+    ms_total = sum(map(sum, per_call_ms)) if flush is not None else start.elapsed_time(stop)
 
     # end to end with pinned host buffers (fewer steps: host copies dominate)
     wk.e2e_setup()

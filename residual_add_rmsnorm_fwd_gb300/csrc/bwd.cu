@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
         }
     }
 
+    allow_dependent_launch();
     if (a.partial != nullptr) {
         float *prow = a.partial + (int64_t)blockIdx.x * a.H;
 #pragma unroll
@@ -192,15 +193,17 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
             }
         }
     }
+    allow_dependent_launch();
 }
 
 // dweight_h = sum_{b = 0}^{G-1} partial[b][h].  A CTA covers 32 columns with
 // kReduceSlices warps; warp k sums the contiguous slice of partial rows
-// [k*G/S, (k+1)*G/S) in ascending order, then the slice sums are added in
-// ascending k.  The order depends only on G, so the result is reproducible.
-// Launched as a programmatic dependent of the backward kernel: its CTAs may
-// start early and wait here for that grid's completion and memory flush.
-constexpr int kReduceSlices = 16;
+// [k*G/S, (k+1)*G/S) in ascending order (eight loads in flight at a time,
+// added one after another), then the slice sums are added in ascending k.
+// The order depends only on G, so the result is reproducible.  Launched as a
+// programmatic dependent of the backward kernel: its CTAs may start early
+// and wait here for that grid's completion and memory flush.
+constexpr int kReduceSlices = 32;
 
 __global__ void __launch_bounds__(32 * kReduceSlices)
     dweight_reduce_kernel(const float *__restrict__ partial, int G, int H, float *__restrict__ dweight) {
@@ -211,8 +214,13 @@ __global__ void __launch_bounds__(32 * kReduceSlices)
     float s = 0.0f;
     if (h < H) {
         const int g0 = (int)((int64_t)G * k / kReduceSlices), g1 = (int)((int64_t)G * (k + 1) / kReduceSlices);
-#pragma unroll 4
-        for (int g = g0; g < g1; ++g) s += __ldg(partial + (int64_t)g * H + h);
+        for (int g = g0; g < g1; g += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = g + u < g1 ? __ldg(partial + (int64_t)(g + u) * H + h) : 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s += v[u];
+        }
     }
     part[k][col] = s;
     __syncthreads();

@@ -278,6 +278,13 @@ __device__ __forceinline__ Pack<T, N> fill(T v) {
     return r;
 }
 
+// Programmatic dependent launch: let a grid launched after this one with
+// programmatic stream serialisation start while this grid finishes (the
+// dependent still waits for this grid's completion before reading its output).
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Reductions.  The xor butterfly leaves the bit-identical sum in every lane
 // (each step adds the same two values in either order), so every thread of a
