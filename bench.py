@@ -15,7 +15,12 @@ beside it.
 
 Prints ONE JSON line (rank 0).  Timing: W untimed warm-up steps, then K
 steps between a barrier + synchronize on both sides, CUDA events on the
-launching stream, max over ranks.  The per-step working set (~0.94 GB) is
+launching stream, max over ranks.  The K steps are replays of a CUDA graph
+that holds R steps (R the largest divisor of K up to 10), so the host issues
+no launch per kernel and nothing sits between the kernels.  Per-kernel
+figures (and the roofline of the dominant kernel) come from a second pass
+that brackets every call with CUDA events.  ``--eager`` launches every call
+from the host instead.  The per-step working set (~0.94 GB) is
 larger than L2, so no flush is needed between steps.
 
 ``--impl reference`` times the fp64 CPU oracle (the only other implementation
@@ -426,6 +431,70 @@ def max_over_ranks(v, world):
     return [float(o.item()) for o in out]
 
 
+def replay_divisor(K, cap=10):
+    """Steps per captured graph: the largest divisor of K not above `cap`."""
+    return max(r for r in range(1, min(K, cap) + 1) if K % r == 0)
+
+
+def capture_steps(torch, calls, R, timed_calls):
+    """Capture R steps of `calls` into a CUDA graph.  With `timed_calls`,
+    every call is bracketed by timing events recorded as graph nodes (None
+    when this torch cannot record events inside a capture)."""
+    ev = None
+    if timed_calls:
+        try:
+            ev = [[(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in calls] for _ in range(R)]
+        except TypeError:
+            return None
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for r in range(R):
+                for j, (_, fn, _) in enumerate(calls):
+                    if ev is not None:
+                        ev[r][j][0].record()
+                    fn()
+                    if ev is not None:
+                        ev[r][j][1].record()
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()                      # one untimed replay
+    torch.cuda.synchronize()
+    return g, ev, R
+
+
+def time_calls(torch, calls, stream, n_steps, graph_ok, flush=None):
+    """Per-call durations (ms), each call bracketed by CUDA events on the
+    launching stream: a graph with event nodes replayed step by step, or
+    eager launches (with an L2 flush before every step when `flush`)."""
+    samples = [[] for _ in calls]
+    cap = capture_steps(torch, calls, 1, True) if (graph_ok and flush is None) else None
+    if cap is not None:
+        g, ev, _ = cap
+        for _ in range(n_steps):
+            g.replay()
+            torch.cuda.synchronize()
+            for j in range(len(calls)):
+                samples[j].append(ev[0][j][0].elapsed_time(ev[0][j][1]))
+        return samples
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+          for _ in range(n_steps)]
+    for k in range(n_steps):
+        if flush is not None:
+            flush.fill_(k & 0xFF)
+        for j, (_, fn, _) in enumerate(calls):
+            ev[k][j][0].record(stream)
+            fn()
+            ev[k][j][1].record(stream)
+    torch.cuda.synchronize()
+    for k in range(n_steps):
+        for j in range(len(calls)):
+            samples[j].append(ev[k][j][0].elapsed_time(ev[k][j][1]))
+    return samples
+
+
 def run_native(args):
     import torch
     rank, world, local = dist_setup(args.gpus)
@@ -439,29 +508,45 @@ def run_native(args):
 
     K = args.steps
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if wk.flush_l2 else None
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
-          for _ in range(K)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph = None
+    if args.graph and flush is None:
+        graph = capture_steps(torch, calls, replay_divisor(K), False)
     sampler = ClockSampler(local).start() if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
-    start.record(stream)
-    for k in range(K):
-        if flush is not None:
-            flush.fill_(k & 0xFF)
-        for j, (_, fn, _) in enumerate(calls):
-            ev[k][j][0].record(stream)
-            fn()
-            ev[k][j][1].record(stream)
-    stop.record(stream)
-    torch.cuda.synchronize()
+    flush_ms = 0.0
+    if graph is not None:
+        # the timed region: a CUDA graph of R steps replayed K / R times, no
+        # host work and no timing nodes between the kernels
+        g, _, R = graph
+        start.record(stream)
+        for _ in range(K // R):
+            g.replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+    else:
+        fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        start.record(stream)
+        for k in range(K):
+            if flush is not None:
+                fe[k][0].record(stream)
+                flush.fill_(k & 0xFF)
+                fe[k][1].record(stream)
+            for _, fn, _ in calls:
+                fn()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if flush is not None:   # the L2 flushes are not part of the step
+            flush_ms = sum(a.elapsed_time(b) for a, b in fe)
     t1 = time.time()
     barrier(world)
-    per_call_ms = [[ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(K)] for j in range(len(calls))]
-    # with L2 flushes in the timed region, only the calls' own intervals count
-    ms_total = sum(map(sum, per_call_ms)) if flush is not None else start.elapsed_time(stop)
+    ms_total = start.elapsed_time(stop) - flush_ms
+    # per-kernel durations: a second pass with CUDA events around every call
+    n_kernel_steps = max(1, min(K, 200))
+    per_call_ms = time_calls(torch, calls, stream, n_kernel_steps, args.graph, flush)
 
     # end to end with pinned host buffers (fewer steps: host copies dominate)
     wk.e2e_setup()
@@ -498,7 +583,7 @@ def run_native(args):
                        "median_us": statistics.median(samples) * 1e3,
                        "gbs": nbytes / (avg / 1e3) / 1e9, "algorithmic_bytes": nbytes,
                        "frac_of_measured_peak": nbytes / (avg / 1e3) / 1e9 / peak,
-                       "share_of_step": sum(samples) / ms_total}
+                       "share_of_step": avg * len(idx) / (ms_total / K)}
     dom = max(kern, key=lambda k: kern[k]["share_of_step"])
     traffic = profile_traffic(f"{dom}_{wk.dt}_{wk.M}x{wk.H}")
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(kern[dom]["gbs"], 1), "peak": peak,
@@ -517,6 +602,10 @@ def run_native(args):
         "e2e": {"value": round(agg_e2e["gbs"], 2), "unit": "GB/s", "h2d_bytes_per_step": wk.h2d,
                 "d2h_bytes_per_step": wk.d2h, "ms_per_step": round(agg_e2e["ms"], 4), "steps": Ke},
         "gpu_launches": K * wk.kernels_per_step,
+        "launch_mode": (f"CUDA graph of {graph[2]} steps replayed {K // graph[2]} times" if graph is not None
+                        else "eager launches"),
+        "kernel_timing": (f"{n_kernel_steps} further steps with CUDA events around every call on the launching "
+                          "stream (events add a short launch bubble, so per-kernel times are upper bounds)"),
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
@@ -584,6 +673,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", dest="graph", action="store_false",
+                    help="time eager launches instead of CUDA-graph replays")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -89,7 +89,6 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
         }
     }
 
-    allow_dependent_launch();
     if (a.partial != nullptr) {
         float *prow = a.partial + (int64_t)blockIdx.x * a.H;
 #pragma unroll
@@ -193,7 +192,6 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
             }
         }
     }
-    allow_dependent_launch();
 }
 
 // dweight_h = sum_{b = 0}^{G-1} partial[b][h].  A CTA covers 32 columns with
@@ -207,7 +205,6 @@ constexpr int kReduceSlices = 32;
 
 __global__ void __launch_bounds__(32 * kReduceSlices)
     dweight_reduce_kernel(const float *__restrict__ partial, int G, int H, float *__restrict__ dweight) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float part[kReduceSlices][33];
     const int col = threadIdx.x & 31, k = threadIdx.x >> 5;
     const int h = blockIdx.x * 32 + col;
@@ -339,17 +336,8 @@ cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, 
     e = cudaLaunchKernel(k, dim3((unsigned)p.grid), dim3((unsigned)p.threads), params, p.smem_bytes, st);
     if (e != cudaSuccess) return e;
     if (dweight != nullptr && a.partial != nullptr) {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3((unsigned)((a.H + 31) / 32));
-        cfg.blockDim = dim3(32 * kReduceSlices);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, dweight_reduce_kernel, (const float *)a.partial, p.grid, a.H, dweight);
+        e = launch_kernel(dweight_reduce_kernel, (unsigned)((a.H + 31) / 32), 32 * kReduceSlices, 0, st,
+                       (const float *)a.partial, p.grid, a.H, dweight);
     }
     return e;
 }

@@ -120,7 +120,6 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
         }
     }
 
-    allow_dependent_launch();
     if (a.partial != nullptr) {
         float *prow = a.partial + (int64_t)blockIdx.x * a.H;
 #pragma unroll

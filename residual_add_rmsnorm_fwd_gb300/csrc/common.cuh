@@ -278,13 +278,6 @@ __device__ __forceinline__ Pack<T, N> fill(T v) {
     return r;
 }
 
-// Programmatic dependent launch: let a grid launched after this one with
-// programmatic stream serialisation start while this grid finishes (the
-// dependent still waits for this grid's completion before reading its output).
-__device__ __forceinline__ void allow_dependent_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Reductions.  The xor butterfly leaves the bit-identical sum in every lane
 // (each step adds the same two values in either order), so every thread of a
@@ -310,6 +303,23 @@ __device__ __forceinline__ float block_sum(float v, float *red, int bank) {
     const int nwarps = blockDim.x >> 5;
     float t = lane < nwarps ? buf[lane] : 0.0f;
     return group_sum<32>(t);
+}
+
+// Sums over the CTA of U values at once, behind one barrier.  `red` holds
+// two banks of U * 32 floats, alternated as for block_sum.
+template <int U>
+__device__ __forceinline__ void block_sum_n(float (&v)[U], float *red, int bank) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *buf = red + bank * U * 32;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        v[u] = group_sum<32>(v[u]);
+        if (lane == 0) buf[u * 32 + warp] = v[u];
+    }
+    __syncthreads();
+    const int nwarps = blockDim.x >> 5;
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = group_sum<32>(lane < nwarps ? buf[u * 32 + lane] : 0.0f);
 }
 
 }  // namespace rmsn

@@ -105,8 +105,7 @@ cudaError_t launch_t(const FwdArgs &a, int sm_count, cudaStream_t st) {
     const int occ = occupancy(reinterpret_cast<const void *>(k), kThreads, 0);
     if (occ <= 0) return cudaErrorInvalidConfiguration;
     const int64_t cap = (int64_t)occ * sm_count;
-    k<<<(unsigned)(a.M < cap ? a.M : cap), kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k, (unsigned)(a.M < cap ? a.M : cap), kThreads, 0, st, a);
 }
 
 template <typename T>

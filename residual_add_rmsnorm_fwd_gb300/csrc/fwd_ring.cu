@@ -133,8 +133,7 @@ cudaError_t launch_t(const FwdArgs &a, const RingPlan &p, cudaStream_t st) {
     auto k = fwd_ring_kernel<T, NV, RESID>;
     cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(k), p.smem_bytes);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)p.grid, p.threads, p.smem_bytes, st>>>(a, p.shape);
-    return cudaGetLastError();
+    return launch_kernel(k, (unsigned)p.grid, (unsigned)p.threads, p.smem_bytes, st, a, p.shape);
 }
 
 template <typename T, bool RESID>

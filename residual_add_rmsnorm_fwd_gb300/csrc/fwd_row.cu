@@ -13,10 +13,10 @@
 
 namespace rmsn {
 
-template <typename T, int VEC, int NV, bool RESID>
+template <typename T, int VEC, int NV, bool RESID, int U>
 __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
     using P = Pack<T, VEC>;
-    __shared__ float red[64];
+    __shared__ float red[2 * U * 32];
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
@@ -33,60 +33,79 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
         wp[i] = (a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
     }
 
+    // U consecutive rows per pass: all their loads are issued before any
+    // arithmetic, and their U sums share one CTA barrier
     int bank = 0;
-    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
-        const int64_t base = row * a.stride;
-        P xp[NV], rp[NV];
+    const int64_t groups = (a.M + U - 1) / U;
+    for (int64_t grp = blockIdx.x; grp < groups; grp += gridDim.x) {
+        P xp[U][NV], rp[U][NV];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int c = threadIdx.x + i * blockDim.x;
-            if (c < nvec) {
-                xp[i] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
-                if constexpr (RESID) rp[i] = ld_stream<T, VEC>(r + base + (int64_t)c * VEC);
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = grp * U + u;
+            const int64_t base = row * a.stride;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int c = threadIdx.x + i * blockDim.x;
+                if (row < a.M && c < nvec) {
+                    xp[u][i] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
+                    if constexpr (RESID) rp[u][i] = ld_stream<T, VEC>(r + base + (int64_t)c * VEC);
+                }
             }
         }
         // binary32 sum of squares (residual added in binary32 first); the
         // post-add sum is written back as the next residual stream
-        float ss = 0.0f;
+        float ss[U];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int c = threadIdx.x + i * blockDim.x;
-            if (c < nvec) {
-                float v[VEC];
-                unpack(xp[i], v);
-                if constexpr (RESID) {
-                    float rv[VEC];
-                    unpack(rp[i], rv);
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = grp * U + u;
+            const int64_t base = row * a.stride;
+            ss[u] = 0.0f;
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
-                    st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
+            for (int i = 0; i < NV; ++i) {
+                const int c = threadIdx.x + i * blockDim.x;
+                if (row < a.M && c < nvec) {
+                    float v[VEC];
+                    unpack(xp[u][i], v);
+                    if constexpr (RESID) {
+                        float rv[VEC];
+                        unpack(rp[u][i], rv);
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                        st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
+                    }
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) ss[u] += v[j] * v[j];
                 }
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) ss += v[j] * v[j];
             }
         }
-        const float total = block_sum(ss, red, bank);
+        block_sum_n<U>(ss, red, bank);
         bank ^= 1;
-        // mean over the full row length, eps inside the square root
-        const float rrms = rsqrtf(total / hf + a.eps);
-        if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[row] = rrms;
-        // y = (s * rrms) * w, one rounding to the storage type
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int c = threadIdx.x + i * blockDim.x;
-            if (c < nvec) {
-                float v[VEC], wv[VEC];
-                unpack(xp[i], v);
-                if constexpr (RESID) {
-                    float rv[VEC];
-                    unpack(rp[i], rv);
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = grp * U + u;
+            if (row >= a.M) continue;
+            const int64_t base = row * a.stride;
+            // mean over the full row length, eps inside the square root
+            const float rrms = rsqrtf(ss[u] / hf + a.eps);
+            if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[row] = rrms;
+            // y = (s * rrms) * w, one rounding to the storage type
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+            for (int i = 0; i < NV; ++i) {
+                const int c = threadIdx.x + i * blockDim.x;
+                if (c < nvec) {
+                    float v[VEC], wv[VEC];
+                    unpack(xp[u][i], v);
+                    if constexpr (RESID) {
+                        float rv[VEC];
+                        unpack(rp[u][i], rv);
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                    }
+                    unpack(wp[i], wv);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
+                    st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
                 }
-                unpack(wp[i], wv);
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
-                st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
             }
         }
     }
@@ -119,14 +138,22 @@ bool pick(int nvec, bool vec, int &threads, int &nv) {
     return false;
 }
 
+// Rows per pass: two for vector rows of at most 4 KB (more bytes in flight
+// per thread), one otherwise.
+template <int VEC, int NV>
+constexpr int rows_per_pass() {
+    return (VEC > 1 && NV <= 2) ? 2 : 1;
+}
+
 template <typename T, int VEC, int NV, bool RESID>
 cudaError_t launch_t(const FwdArgs &a, int threads, int sm_count, cudaStream_t st) {
-    auto k = fwd_row_kernel<T, VEC, NV, RESID>;
+    constexpr int U = rows_per_pass<VEC, NV>();
+    auto k = fwd_row_kernel<T, VEC, NV, RESID, U>;
     const int occ = occupancy(reinterpret_cast<const void *>(k), threads, 0);
     if (occ <= 0) return cudaErrorInvalidConfiguration;
-    const int64_t grid = a.M < (int64_t)occ * sm_count ? a.M : (int64_t)occ * sm_count;
-    k<<<(unsigned)grid, threads, 0, st>>>(a);
-    return cudaGetLastError();
+    const int64_t groups = (a.M + U - 1) / U;
+    const int64_t grid = groups < (int64_t)occ * sm_count ? groups : (int64_t)occ * sm_count;
+    return launch_kernel(k, (unsigned)grid, (unsigned)threads, 0, st, a);
 }
 
 template <typename T, int VEC, bool RESID>

@@ -5,18 +5,21 @@
 // barrier per row, so each row is handled by an aligned group of LANES lanes
 // of one warp (LANES = 1..32, the smallest power of two covering the row's
 // 128-bit vectors, or its elements on the scalar path).  A warp processes
-// 32 / LANES rows at once and reduces each row with xor shuffles that stay
+// 32 / LANES rows at a time and reduces each row with xor shuffles that stay
 // inside its lane group: no shared memory, no barrier.  (The page advises
 // warp-level reductions for hidden sizes below 256: "Skill: Write a Triton
-// RMSNorm Kernel", Do not use this when, third bullet.)
+// RMSNorm Kernel", Do not use this when, third bullet.)  Each lane group
+// takes U consecutive row slots per pass and issues all their loads before
+// any arithmetic, so U 16-byte loads per lane are in flight at once: with a
+// 128-byte row, one row per lane group would leave HBM under-occupied.
 #include "launch.h"
 
 namespace rmsn {
 
-template <typename T, int VEC, int LANES, int NPL, bool RESID>
+template <typename T, int VEC, int LANES, int NPL, bool RESID, int U>
 __global__ void __launch_bounds__(256) fwd_small_kernel(FwdArgs a) {
     using P = Pack<T, VEC>;
-    constexpr int RPW = 32 / LANES;  // rows per warp
+    constexpr int RPW = 32 / LANES;  // rows per warp per slot
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
@@ -37,57 +40,66 @@ __global__ void __launch_bounds__(256) fwd_small_kernel(FwdArgs a) {
 
     const int64_t warps_per_grid = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t warp_id = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    constexpr int ROWS = RPW * U;    // rows per warp per pass
     // warp-uniform loop: every lane takes part in the shuffles
-    for (int64_t row0 = warp_id * RPW; row0 < a.M; row0 += warps_per_grid * RPW) {
-        const int64_t row = row0 + slot;
-        const bool live = row < a.M;
-        const int64_t base = row * a.stride;
-        P xp[NPL], rp[NPL];
+    for (int64_t row0 = warp_id * ROWS; row0 < a.M; row0 += warps_per_grid * ROWS) {
+        P xp[U][NPL], rp[U][NPL];
 #pragma unroll
-        for (int k = 0; k < NPL; ++k) {
-            const int c = li + k * LANES;
-            if (live && c < nvec) {
-                xp[k] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
-                if constexpr (RESID) rp[k] = ld_stream<T, VEC>(r + base + (int64_t)c * VEC);
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = row0 + u * RPW + slot;
+            const int64_t base = row * a.stride;
+#pragma unroll
+            for (int k = 0; k < NPL; ++k) {
+                const int c = li + k * LANES;
+                if (row < a.M && c < nvec) {
+                    xp[u][k] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
+                    if constexpr (RESID) rp[u][k] = ld_stream<T, VEC>(r + base + (int64_t)c * VEC);
+                }
             }
         }
-        float ss = 0.0f;
 #pragma unroll
-        for (int k = 0; k < NPL; ++k) {
-            const int c = li + k * LANES;
-            if (live && c < nvec) {
-                float v[VEC];
-                unpack(xp[k], v);
-                if constexpr (RESID) {
-                    float rv[VEC];
-                    unpack(rp[k], rv);
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = row0 + u * RPW + slot;
+            const bool live = row < a.M;
+            const int64_t base = row * a.stride;
+            float ss = 0.0f;
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
-                    st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
+            for (int k = 0; k < NPL; ++k) {
+                const int c = li + k * LANES;
+                if (live && c < nvec) {
+                    float v[VEC];
+                    unpack(xp[u][k], v);
+                    if constexpr (RESID) {
+                        float rv[VEC];
+                        unpack(rp[u][k], rv);
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                        st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
+                    }
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) ss += v[j] * v[j];
                 }
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) ss += v[j] * v[j];
             }
-        }
-        const float total = group_sum<LANES>(ss);
-        const float rrms = rsqrtf(total / hf + a.eps);
-        if (live && li == 0 && a.rrms != nullptr) a.rrms[row] = rrms;
+            const float total = group_sum<LANES>(ss);
+            const float rrms = rsqrtf(total / hf + a.eps);
+            if (live && li == 0 && a.rrms != nullptr) a.rrms[row] = rrms;
 #pragma unroll
-        for (int k = 0; k < NPL; ++k) {
-            const int c = li + k * LANES;
-            if (live && c < nvec) {
-                float v[VEC], wv[VEC];
-                unpack(xp[k], v);
-                if constexpr (RESID) {
-                    float rv[VEC];
-                    unpack(rp[k], rv);
+            for (int k = 0; k < NPL; ++k) {
+                const int c = li + k * LANES;
+                if (live && c < nvec) {
+                    float v[VEC], wv[VEC];
+                    unpack(xp[u][k], v);
+                    if constexpr (RESID) {
+                        float rv[VEC];
+                        unpack(rp[u][k], rv);
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                    }
+                    unpack(wp[k], wv);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
+                    st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
                 }
-                unpack(wp[k], wv);
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
-                st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
             }
         }
     }
@@ -97,16 +109,23 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Row slots per lane group per pass: enough that each lane has about four
+// 16-byte (or eight scalar) loads in flight.
+template <int VEC, int NPL>
+constexpr int slots() {
+    return VEC > 1 ? (NPL >= 4 ? 1 : 4 / NPL) : (NPL >= 8 ? 1 : 8 / NPL);
+}
+
 template <typename T, int VEC, int LANES, int NPL, bool RESID>
 cudaError_t launch_t(const FwdArgs &a, int sm_count, cudaStream_t st) {
-    auto k = fwd_small_kernel<T, VEC, LANES, NPL, RESID>;
+    constexpr int U = slots<VEC, NPL>();
+    auto k = fwd_small_kernel<T, VEC, LANES, NPL, RESID, U>;
     const int occ = occupancy(reinterpret_cast<const void *>(k), kThreads, 0);
     if (occ <= 0) return cudaErrorInvalidConfiguration;
-    constexpr int rows_per_cta = (kThreads / 32) * (32 / LANES);
+    constexpr int rows_per_cta = (kThreads / 32) * (32 / LANES) * U;
     const int64_t need = (a.M + rows_per_cta - 1) / rows_per_cta;
     const int64_t cap = (int64_t)occ * sm_count;
-    k<<<(unsigned)(need < cap ? need : cap), kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k, (unsigned)(need < cap ? need : cap), kThreads, 0, st, a);
 }
 
 template <typename T, int VEC, bool RESID>
