@@ -196,42 +196,51 @@ class StepWorkload:
         self.host = wl.generate(cfg_id, with_dy=backward)
         self.kernels_per_step = 1 + (2 if backward else 0)
 
-    def setup(self):
+    def _make_set(self):
+        """One set of device buffers (inputs uploaded, outputs allocated)."""
+        from types import SimpleNamespace
         torch, wl, dt = self.torch, self.wl, self.dt
         tdt = wl.torch_dtype(dt)
         dev = torch.device("cuda")
+        M, H, S = self.M, self.H, self.S
 
         def up(a):
-            return wl.to_torch(a, dt).to(dev)
+            return wl.to_torch(a, dt).to(dev)[:, :H]
 
-        M, H, S = self.M, self.H, self.S
-        self.x = up(self.host["x"])[:, :H]
-        self.r = up(self.host["residual"])[:, :H] if self.fused else None
-        self.w = up(self.host["w"])
-        self.y = torch.empty(M, S, dtype=tdt, device=dev)[:, :H]
-        self.s = torch.empty(M, S, dtype=tdt, device=dev)[:, :H] if self.fused else None
-        self.rrms = torch.empty(M, device=dev) if self.backward else None
+        def out():
+            return torch.empty(M, S, dtype=tdt, device=dev)[:, :H]
+
+        b = SimpleNamespace()
+        b.x = up(self.host["x"])
+        b.r = up(self.host["residual"]) if self.fused else None
+        b.y = out()
+        b.s = out() if self.fused else None
+        b.rrms = torch.empty(M, device=dev) if self.backward else None
         if self.backward:
-            self.dy = up(self.host["dy"])[:, :H]
-            self.dx = torch.empty(M, S, dtype=tdt, device=dev)[:, :H]
-            self.dw = torch.empty(H, device=dev)
-            self.ws = torch.empty(max(1, self.rn.rmsnorm_bwd_workspace_bytes(M, H, tdt)), dtype=torch.uint8,
-                                  device=dev)
+            b.dy = up(self.host["dy"])
+            b.dx = out()
+            b.dw = torch.empty(H, device=dev)
+            b.ws = torch.empty(max(1, self.rn.rmsnorm_bwd_workspace_bytes(M, H, tdt)), dtype=torch.uint8,
+                               device=dev)
+        return b
+
+    def setup(self):
+        self.w = self.wl.to_torch(self.host["w"], self.dt).to(self.torch.device("cuda"))
+        self.sets = [self._make_set()]
         return self
 
-    def calls(self):
-        """[(label, fn, algorithmic bytes)] enqueued on the current stream, in order."""
-        rn, eps = self.rn, self.c["eps"]
+    def calls(self, k=0):
+        """[(label, fn, algorithmic bytes)] on buffer set k, enqueued on the current stream, in order."""
+        rn, eps, b = self.rn, self.c["eps"], self.sets[k]
         out = []
         if self.fused:
-            out.append(("fwd_residual", lambda: rn.rmsnorm_fwd_residual(self.x, self.r, self.w, self.y, self.s,
-                                                                        self.rrms, eps=eps), self.fwd_bytes))
+            out.append(("fwd_residual", lambda: rn.rmsnorm_fwd_residual(b.x, b.r, self.w, b.y, b.s, b.rrms, eps=eps),
+                        self.fwd_bytes))
         else:
-            out.append(("fwd", lambda: rn.rmsnorm_fwd(self.x, self.w, self.y, self.rrms, eps=eps), self.fwd_bytes))
+            out.append(("fwd", lambda: rn.rmsnorm_fwd(b.x, self.w, b.y, b.rrms, eps=eps), self.fwd_bytes))
         if self.backward:
-            xin = self.s if self.fused else self.x
-            out.append(("bwd", lambda: rn.rmsnorm_bwd(self.dy, xin, self.w, self.rrms, self.dx, self.dw, self.ws),
-                        self.bwd_bytes))
+            xin = b.s if self.fused else b.x
+            out.append(("bwd", lambda: rn.rmsnorm_bwd(b.dy, xin, self.w, b.rrms, b.dx, b.dw, b.ws), self.bwd_bytes))
         return out
 
     def config(self):
@@ -244,38 +253,27 @@ class StepWorkload:
             cfg.update(B=8, T=2048)
         return cfg
 
-    # end to end through the binding with pinned host buffers
+    # end to end through the binding: pinned host inputs and outputs, two
+    # device buffer sets so that copies of one step overlap another's kernels
     def e2e_setup(self):
-        torch = self.torch
+        torch, b = self.torch, self.sets[0]
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
-        self.hx = self.wl.to_torch(self.host["x"], self.dt)[:, :self.H].contiguous().pin_memory()
-        self.hr = (self.wl.to_torch(self.host["residual"], self.dt)[:, :self.H].contiguous().pin_memory()
-                   if self.fused else None)
-        self.hdy = (self.wl.to_torch(self.host["dy"], self.dt)[:, :self.H].contiguous().pin_memory()
-                    if self.backward else None)
-        self.hy = pin(self.y)
-        self.hs = pin(self.s) if self.fused else None
-        self.hdx = pin(self.dx) if self.backward else None
-        self.hdw = pin(self.dw) if self.backward else None
-        ins = [t for t in (self.hx, self.hr, self.hdy) if t is not None]
-        outs = [t for t in (self.hy, self.hs, self.hdx, self.hdw) if t is not None]
-        self.h2d = sum(t.numel() * t.element_size() for t in ins)
-        self.d2h = sum(t.numel() * t.element_size() for t in outs)
+        host = lambda a: self.wl.to_torch(a, self.dt)[:, :self.H].contiguous().pin_memory()  # noqa: E731
+        self.h_in = [host(self.host["x"])] + ([host(self.host["residual"])] if self.fused else []) + \
+            ([host(self.host["dy"])] if self.backward else [])
+        outs = [b.y] + ([b.s] if self.fused else []) + ([b.dx, b.dw] if self.backward else [])
+        self.h_out = [pin(t) for t in outs]
+        while len(self.sets) < 2:
+            self.sets.append(self._make_set())
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h_in)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
 
-    def e2e_step(self):
-        self.x.copy_(self.hx, non_blocking=True)
-        if self.fused:
-            self.r.copy_(self.hr, non_blocking=True)
-        if self.backward:
-            self.dy.copy_(self.hdy, non_blocking=True)
-        for _, fn, _ in self.calls():
-            fn()
-        self.hy.copy_(self.y, non_blocking=True)
-        if self.fused:
-            self.hs.copy_(self.s, non_blocking=True)
-        if self.backward:
-            self.hdx.copy_(self.dx, non_blocking=True)
-            self.hdw.copy_(self.dw, non_blocking=True)
+    def e2e_transfers(self, k):
+        """([(device, host)] inputs, [(host, device)] results) of buffer set k."""
+        b = self.sets[k]
+        dev_in = [b.x] + ([b.r] if self.fused else []) + ([b.dy] if self.backward else [])
+        dev_out = [b.y] + ([b.s] if self.fused else []) + ([b.dx, b.dw] if self.backward else [])
+        return list(zip(dev_in, self.h_in)), list(zip(self.h_out, dev_out))
 
     # CPU oracle on a row sample of the same inputs
     def oracle_step(self, rows):
@@ -318,30 +316,37 @@ class DitMixWorkload:
         self.rows_per_step = self.n_calls * self.M + c["head_M"]
         self.kernels_per_step = self.n_calls + 1
 
-    def setup(self):
+    def _make_set(self):
+        from types import SimpleNamespace
         torch, wl, dt = self.torch, self.wl, self.dt
         dev = torch.device("cuda")
-        self.xs = [wl.to_torch(a, dt).to(dev) for a in self.host["xs"]]
-        self.ys = [torch.empty_like(x) for x in self.xs]
-        self.w = wl.to_torch(self.host["w"], dt).to(dev)
-        self.hx = wl.to_torch(self.host["head_x"], dt).to(dev)
-        self.hy = torch.empty_like(self.hx)
-        self.hw = wl.to_torch(self.host["head_w"], dt).to(dev)
+        b = SimpleNamespace()
+        b.xs = [wl.to_torch(a, dt).to(dev) for a in self.host["xs"]]
+        b.ys = [torch.empty_like(x) for x in b.xs]
+        b.hx = wl.to_torch(self.host["head_x"], dt).to(dev)
+        b.hy = torch.empty_like(b.hx)
+        return b
+
+    def setup(self):
+        dev = self.torch.device("cuda")
+        self.w = self.wl.to_torch(self.host["w"], self.dt).to(dev)
+        self.hw = self.wl.to_torch(self.host["head_w"], self.dt).to(dev)
+        self.sets = [self._make_set()]
         return self
 
-    def calls(self):
-        rn, eps, nb = self.rn, self.c["eps"], len(self.xs)
+    def calls(self, k=0):
+        rn, eps, b = self.rn, self.c["eps"], self.sets[k]
+        nb = len(b.xs)
         out = []
         for i in range(self.n_calls):
-            x, y = self.xs[i % nb], self.ys[i % nb]
+            x, y = b.xs[i % nb], b.ys[i % nb]
             if i % 3 == 0:   # one call in three has a weight: 56 of 168
                 out.append(("fwd_2048_weighted", lambda x=x, y=y: rn.rmsnorm_fwd(x, self.w, y, None, eps=eps),
                             self.call_bytes_w))
             else:
                 out.append(("fwd_2048_unweighted", lambda x=x, y=y: rn.rmsnorm_fwd(x, None, y, None, eps=eps),
                             self.call_bytes_nw))
-        out.append(("fwd_heads_64", lambda: rn.rmsnorm_fwd(self.hx, self.hw, self.hy, None, eps=eps),
-                    self.head_bytes))
+        out.append(("fwd_heads_64", lambda: rn.rmsnorm_fwd(b.hx, self.hw, b.hy, None, eps=eps), self.head_bytes))
         return out
 
     def config(self):
@@ -349,23 +354,21 @@ class DitMixWorkload:
         return {"workload": self.name, "M": self.M, "H": self.H, "dtype": self.dt, "calls_per_step": self.n_calls,
                 "weighted_calls": c["calls_weighted"], "unweighted_calls": c["calls_unweighted"],
                 "head_M": c["head_M"], "head_H": c["head_H"], "eps": c["eps"],
-                "l2": f"{len(self.xs)} rotating x/y buffer sets of {2 * self.M * self.H * self.es} bytes",
+                "l2": f"{len(self.sets[0].xs)} rotating x/y buffer sets of {2 * self.M * self.H * self.es} bytes",
                 "algorithmic_bytes_per_step": self.bytes_per_step}
 
     def e2e_setup(self):
-        torch = self.torch
-        self.h_in = [x.cpu().pin_memory() for x in self.xs] + [self.hx.cpu().pin_memory()]
-        self.h_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in self.ys + [self.hy]]
+        torch, b = self.torch, self.sets[0]
+        self.h_in = [x.cpu().pin_memory() for x in b.xs] + [b.hx.cpu().pin_memory()]
+        self.h_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in b.ys + [b.hy]]
+        while len(self.sets) < 2:
+            self.sets.append(self._make_set())
         self.h2d = sum(t.numel() * t.element_size() for t in self.h_in)
         self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
 
-    def e2e_step(self):
-        for d, h in zip(self.xs + [self.hx], self.h_in):
-            d.copy_(h, non_blocking=True)
-        for _, fn, _ in self.calls():
-            fn()
-        for h, d in zip(self.h_out, self.ys + [self.hy]):
-            h.copy_(d, non_blocking=True)
+    def e2e_transfers(self, k):
+        b = self.sets[k]
+        return list(zip(b.xs + [b.hx], self.h_in)), list(zip(self.h_out, b.ys + [b.hy]))
 
     def oracle_step(self, rows):
         import oracle
@@ -495,6 +498,62 @@ def time_calls(torch, calls, stream, n_steps, graph_ok, flush=None):
     return samples
 
 
+def run_e2e(torch, wk, K, world):
+    """ms per step end to end: every step copies its inputs from pinned host
+    memory, runs the calls through the binding and copies its results back.
+    Two device buffer sets and three streams (upload, compute, download) let
+    step k's copies overlap step k-1's kernels and each other; events keep a
+    set's inputs until its kernels consumed them and its outputs until they
+    were copied out."""
+    wk.e2e_setup()
+    comp, up, down = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    nset = 2
+    up_done = [torch.cuda.Event() for _ in range(nset)]
+    comp_done = [torch.cuda.Event() for _ in range(nset)]
+    down_done = [torch.cuda.Event() for _ in range(nset)]
+    calls = [wk.calls(b) for b in range(nset)]
+    transfers = [wk.e2e_transfers(b) for b in range(nset)]
+
+    def step(k):
+        b = k % nset
+        h2d, d2h = transfers[b]
+        if k >= nset:
+            up.wait_event(comp_done[b])        # set b's inputs were consumed
+        with torch.cuda.stream(up):
+            for dev, host in h2d:
+                dev.copy_(host, non_blocking=True)
+            up_done[b].record(up)
+        comp.wait_event(up_done[b])
+        if k >= nset:
+            comp.wait_event(down_done[b])      # set b's results were copied out
+        for _, fn, _ in calls[b]:
+            fn()
+        comp_done[b].record(comp)
+        down.wait_event(comp_done[b])
+        with torch.cuda.stream(down):
+            for host, dev in d2h:
+                host.copy_(dev, non_blocking=True)
+            down_done[b].record(down)
+
+    k = 0
+    for _ in range(2):
+        step(k)
+        k += 1
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    up.wait_event(e0)
+    for _ in range(K):
+        step(k)
+        k += 1
+    comp.wait_event(down_done[(k - 1) % nset])
+    e1.record(comp)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / K
+
+
 def run_native(args):
     import torch
     rank, world, local = dist_setup(args.gpus)
@@ -549,20 +608,8 @@ def run_native(args):
     per_call_ms = time_calls(torch, calls, stream, n_kernel_steps, args.graph, flush)
 
     # end to end with pinned host buffers (fewer steps: host copies dominate)
-    wk.e2e_setup()
     Ke = max(3, min(K, 20))
-    for _ in range(2):
-        wk.e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(Ke):
-        wk.e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = e0.elapsed_time(e1) / Ke
+    e2e_ms = run_e2e(torch, wk, Ke, world)
 
     clocks = summarize_clocks(sampler.stop(), t0, t1) if sampler else None
     all_ms = max_over_ranks(ms_total / K, world)
@@ -600,7 +647,8 @@ def run_native(args):
                     for k, v in kern.items()},
         "roofline": roofline,
         "e2e": {"value": round(agg_e2e["gbs"], 2), "unit": "GB/s", "h2d_bytes_per_step": wk.h2d,
-                "d2h_bytes_per_step": wk.d2h, "ms_per_step": round(agg_e2e["ms"], 4), "steps": Ke},
+                "d2h_bytes_per_step": wk.d2h, "ms_per_step": round(agg_e2e["ms"], 4), "steps": Ke,
+                "mode": "pinned host buffers; 2 device buffer sets; upload, compute, download streams overlap"},
         "gpu_launches": K * wk.kernels_per_step,
         "launch_mode": (f"CUDA graph of {graph[2]} steps replayed {K // graph[2]} times" if graph is not None
                         else "eager launches"),
