@@ -138,22 +138,34 @@ bool pick(int nvec, bool vec, int &threads, int &nv) {
     return false;
 }
 
-// Rows per pass: two for vector rows of at most 4 KB (more bytes in flight
-// per thread), one otherwise.
-template <int VEC, int NV>
-constexpr int rows_per_pass() {
-    return (VEC > 1 && NV <= 2) ? 2 : 1;
+template <typename T, int VEC, int NV, bool RESID, int U>
+cudaError_t launch_u(const FwdArgs &a, int threads, int64_t grid, cudaStream_t st) {
+    return launch_kernel(fwd_row_kernel<T, VEC, NV, RESID, U>, (unsigned)grid, (unsigned)threads, 0, st, a);
 }
 
+// Rows per pass: 2 keeps twice the bytes in flight per thread, but the rows
+// are then dealt out in pairs, which can leave a larger last round (12288
+// rows over 1368 CTAs: 8.98 rounds of one row, 4.49 rounds of two -- ten
+// rows of work for the slowest CTA instead of nine).  Take 2 only for
+// vector rows of at most 4 KB and only when it does not lengthen the
+// slowest CTA's share.
 template <typename T, int VEC, int NV, bool RESID>
 cudaError_t launch_t(const FwdArgs &a, int threads, int sm_count, cudaStream_t st) {
-    constexpr int U = rows_per_pass<VEC, NV>();
-    auto k = fwd_row_kernel<T, VEC, NV, RESID, U>;
-    const int occ = occupancy(reinterpret_cast<const void *>(k), threads, 0);
+    const int occ = occupancy(reinterpret_cast<const void *>(fwd_row_kernel<T, VEC, NV, RESID, 1>), threads, 0);
     if (occ <= 0) return cudaErrorInvalidConfiguration;
-    const int64_t groups = (a.M + U - 1) / U;
-    const int64_t grid = groups < (int64_t)occ * sm_count ? groups : (int64_t)occ * sm_count;
-    return launch_kernel(k, (unsigned)grid, (unsigned)threads, 0, st, a);
+    const int64_t cap = (int64_t)occ * sm_count;
+    auto share = [&](int64_t u) {   // rows handled by the busiest CTA
+        const int64_t groups = (a.M + u - 1) / u;
+        return (groups + cap - 1) / cap * u;
+    };
+    if (VEC > 1 && NV <= 2 && share(2) <= share(1)) {
+        const int occ2 = occupancy(reinterpret_cast<const void *>(fwd_row_kernel<T, VEC, NV, RESID, 2>), threads, 0);
+        if (occ2 >= occ) {
+            const int64_t groups = (a.M + 1) / 2;
+            return launch_u<T, VEC, NV, RESID, 2>(a, threads, groups < cap ? groups : cap, st);
+        }
+    }
+    return launch_u<T, VEC, NV, RESID, 1>(a, threads, a.M < cap ? a.M : cap, st);
 }
 
 template <typename T, int VEC, bool RESID>

@@ -109,23 +109,42 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Row slots per lane group per pass: enough that each lane has about four
-// 16-byte (or eight scalar) loads in flight.
-template <int VEC, int NPL>
-constexpr int slots() {
-    return VEC > 1 ? (NPL >= 4 ? 1 : 4 / NPL) : (NPL >= 8 ? 1 : 8 / NPL);
+template <typename T, int VEC, int LANES, int NPL, bool RESID, int U>
+int64_t resident_ctas(int sm_count) {
+    return (int64_t)occupancy(reinterpret_cast<const void *>(fwd_small_kernel<T, VEC, LANES, NPL, RESID, U>),
+                              kThreads, 0) * sm_count;
 }
 
-template <typename T, int VEC, int LANES, int NPL, bool RESID>
-cudaError_t launch_t(const FwdArgs &a, int sm_count, cudaStream_t st) {
-    constexpr int U = slots<VEC, NPL>();
-    auto k = fwd_small_kernel<T, VEC, LANES, NPL, RESID, U>;
-    const int occ = occupancy(reinterpret_cast<const void *>(k), kThreads, 0);
-    if (occ <= 0) return cudaErrorInvalidConfiguration;
+template <typename T, int VEC, int LANES, int NPL, bool RESID, int U>
+cudaError_t launch_u(const FwdArgs &a, int sm_count, cudaStream_t st) {
+    const int64_t cap = resident_ctas<T, VEC, LANES, NPL, RESID, U>(sm_count);
+    if (cap <= 0) return cudaErrorInvalidConfiguration;
     constexpr int rows_per_cta = (kThreads / 32) * (32 / LANES) * U;
     const int64_t need = (a.M + rows_per_cta - 1) / rows_per_cta;
-    const int64_t cap = (int64_t)occ * sm_count;
-    return launch_kernel(k, (unsigned)(need < cap ? need : cap), kThreads, 0, st, a);
+    return launch_kernel(fwd_small_kernel<T, VEC, LANES, NPL, RESID, U>, (unsigned)(need < cap ? need : cap),
+                         kThreads, 0, st, a);
+}
+
+// Row slots per lane group per pass, U in {1, 2, 4} (at most four 16-byte
+// loads per lane in flight): the largest U that does not lengthen the
+// busiest warp's share of rows.  Warps work independently, so the share is
+// counted in warp passes: 393216 rows of 64 bf16 with four rows per warp
+// pass over 9728 warps is 10.1 passes with U = 1 (11 rows of work per lane
+// group) against 2.53 with U = 4 (12).
+template <typename T, int VEC, int LANES, int NPL, bool RESID>
+cudaError_t launch_t(const FwdArgs &a, int sm_count, cudaStream_t st) {
+    constexpr int RPW = 32 / LANES;
+    auto share = [&](int64_t u, int64_t ctas) {
+        const int64_t warps = ctas * (kThreads / 32);
+        const int64_t passes = (a.M + RPW * u - 1) / (RPW * u);
+        return warps > 0 ? (passes + warps - 1) / warps * u : INT64_MAX;
+    };
+    const int64_t s1 = share(1, resident_ctas<T, VEC, LANES, NPL, RESID, 1>(sm_count));
+    if (NPL == 1 && share(4, resident_ctas<T, VEC, LANES, NPL, RESID, 4>(sm_count)) <= s1)
+        return launch_u<T, VEC, LANES, NPL, RESID, 4>(a, sm_count, st);
+    if (NPL <= 2 && share(2, resident_ctas<T, VEC, LANES, NPL, RESID, 2>(sm_count)) <= s1)
+        return launch_u<T, VEC, LANES, NPL, RESID, 2>(a, sm_count, st);
+    return launch_u<T, VEC, LANES, NPL, RESID, 1>(a, sm_count, st);
 }
 
 template <typename T, int VEC, bool RESID>
