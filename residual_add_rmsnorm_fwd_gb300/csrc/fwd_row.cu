@@ -16,6 +16,10 @@ namespace rmsn {
 template <typename T, int VEC, int NV, bool RESID, int U>
 __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
     using P = Pack<T, VEC>;
+    // 16-byte groups compute on binary32 pairs (two-lane f32x2 instructions);
+    // the scalar path (unaligned rows) one element at a time
+    constexpr bool PAIRS = VEC > 1;
+    constexpr int PR = PAIRS ? VEC / 2 : 1;
     __shared__ float red[2 * U * 32];
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ r = static_cast<const T *>(a.r);
@@ -25,7 +29,9 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;   // exact: H < 2^24
 
-    // weight (H,), indexed by column only; ones when the norm has no weight
+    // weight (H,), indexed by column only; ones when the norm has no weight.
+    // Kept packed (and x, residual too): widening again in the scale step is
+    // cheaper than the registers binary32 copies would take from occupancy.
     P wp[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -60,23 +66,34 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
             const int64_t row = grp * U + u;
             const int64_t base = row * a.stride;
             ss[u] = 0.0f;
+            f32x2 ss2 = f2_make(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 const int c = threadIdx.x + i * blockDim.x;
                 if (row < a.M && c < nvec) {
-                    float v[VEC];
-                    unpack(xp[u][i], v);
-                    if constexpr (RESID) {
-                        float rv[VEC];
-                        unpack(rp[u][i], rv);
+                    if constexpr (PAIRS) {
+                        f32x2 sv[PR];
+                        widen16<T>(xp[u][i], sv);
+                        if constexpr (RESID) {
+                            f32x2 rv[PR];
+                            widen16<T>(rp[u][i], rv);
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
-                        st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
+                            for (int q = 0; q < PR; ++q) sv[q] = f2_add(sv[q], rv[q]);
+                            st_global<T, VEC>(s_out + base + (int64_t)c * VEC, narrow16<T>(sv));
+                        }
+#pragma unroll
+                        for (int q = 0; q < PR; ++q) ss2 = f2_fma(sv[q], sv[q], ss2);
+                    } else {
+                        float v = to_f32(xp[u][i].v[0]);
+                        if constexpr (RESID) {
+                            v += to_f32(rp[u][i].v[0]);
+                            s_out[base + c] = from_f32<T>(v);
+                        }
+                        ss[u] += v * v;
                     }
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) ss[u] += v[j] * v[j];
                 }
             }
+            if constexpr (PAIRS) ss[u] = f2_sum(ss2);
         }
         block_sum_n<U>(ss, red, bank);
         bank ^= 1;
@@ -88,23 +105,30 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
             // mean over the full row length, eps inside the square root
             const float rrms = rsqrtf(ss[u] / hf + a.eps);
             if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[row] = rrms;
+            const f32x2 rr2 = f2_make(rrms, rrms);
             // y = (s * rrms) * w, one rounding to the storage type
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 const int c = threadIdx.x + i * blockDim.x;
                 if (c < nvec) {
-                    float v[VEC], wv[VEC];
-                    unpack(xp[u][i], v);
-                    if constexpr (RESID) {
-                        float rv[VEC];
-                        unpack(rp[u][i], rv);
+                    if constexpr (PAIRS) {
+                        f32x2 sv[PR], wv[PR];
+                        widen16<T>(xp[u][i], sv);
+                        if constexpr (RESID) {
+                            f32x2 rv[PR];
+                            widen16<T>(rp[u][i], rv);
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                            for (int q = 0; q < PR; ++q) sv[q] = f2_add(sv[q], rv[q]);
+                        }
+                        widen16<T>(wp[i], wv);
+#pragma unroll
+                        for (int q = 0; q < PR; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
+                        st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(sv));
+                    } else {
+                        float v = to_f32(xp[u][i].v[0]);
+                        if constexpr (RESID) v += to_f32(rp[u][i].v[0]);
+                        y[base + c] = from_f32<T>((v * rrms) * to_f32(wp[i].v[0]));
                     }
-                    unpack(wp[i], wv);
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
-                    st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
                 }
             }
         }
@@ -158,11 +182,14 @@ cudaError_t launch_t(const FwdArgs &a, int threads, int sm_count, cudaStream_t s
         const int64_t groups = (a.M + u - 1) / u;
         return (groups + cap - 1) / cap * u;
     };
-    if (VEC > 1 && NV <= 2 && share(2) <= share(1)) {
-        const int occ2 = occupancy(reinterpret_cast<const void *>(fwd_row_kernel<T, VEC, NV, RESID, 2>), threads, 0);
-        if (occ2 >= occ) {
-            const int64_t groups = (a.M + 1) / 2;
-            return launch_u<T, VEC, NV, RESID, 2>(a, threads, groups < cap ? groups : cap, st);
+    if constexpr (VEC > 1 && NV <= 2) {
+        if (share(2) <= share(1)) {
+            const int occ2 =
+                occupancy(reinterpret_cast<const void *>(fwd_row_kernel<T, VEC, NV, RESID, 2>), threads, 0);
+            if (occ2 >= occ) {
+                const int64_t groups = (a.M + 1) / 2;
+                return launch_u<T, VEC, NV, RESID, 2>(a, threads, groups < cap ? groups : cap, st);
+            }
         }
     }
     return launch_u<T, VEC, NV, RESID, 1>(a, threads, a.M < cap ? a.M : cap, st);
