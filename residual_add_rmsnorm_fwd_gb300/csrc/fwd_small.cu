@@ -63,42 +63,60 @@ __global__ void __launch_bounds__(256) fwd_small_kernel(FwdArgs a) {
             const bool live = row < a.M;
             const int64_t base = row * a.stride;
             float ss = 0.0f;
+            f32x2 ss2 = f2_make(0.0f, 0.0f);
 #pragma unroll
             for (int k = 0; k < NPL; ++k) {
                 const int c = li + k * LANES;
                 if (live && c < nvec) {
-                    float v[VEC];
-                    unpack(xp[u][k], v);
-                    if constexpr (RESID) {
-                        float rv[VEC];
-                        unpack(rp[u][k], rv);
+                    if constexpr (VEC > 1) {   // binary32 pairs, two lanes per instruction
+                        f32x2 sv[VEC / 2];
+                        widen16<T>(xp[u][k], sv);
+                        if constexpr (RESID) {
+                            f32x2 rv[VEC / 2];
+                            widen16<T>(rp[u][k], rv);
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
-                        st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
+                            for (int q = 0; q < VEC / 2; ++q) sv[q] = f2_add(sv[q], rv[q]);
+                            st_global<T, VEC>(s_out + base + (int64_t)c * VEC, narrow16<T>(sv));
+                        }
+#pragma unroll
+                        for (int q = 0; q < VEC / 2; ++q) ss2 = f2_fma(sv[q], sv[q], ss2);
+                    } else {
+                        float v = to_f32(xp[u][k].v[0]);
+                        if constexpr (RESID) {
+                            v += to_f32(rp[u][k].v[0]);
+                            s_out[base + c] = from_f32<T>(v);
+                        }
+                        ss += v * v;
                     }
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) ss += v[j] * v[j];
                 }
             }
+            if constexpr (VEC > 1) ss = f2_sum(ss2);
             const float total = group_sum<LANES>(ss);
             const float rrms = rsqrtf(total / hf + a.eps);
             if (live && li == 0 && a.rrms != nullptr) a.rrms[row] = rrms;
+            const f32x2 rr2 = f2_make(rrms, rrms);
 #pragma unroll
             for (int k = 0; k < NPL; ++k) {
                 const int c = li + k * LANES;
                 if (live && c < nvec) {
-                    float v[VEC], wv[VEC];
-                    unpack(xp[u][k], v);
-                    if constexpr (RESID) {
-                        float rv[VEC];
-                        unpack(rp[u][k], rv);
+                    if constexpr (VEC > 1) {
+                        f32x2 sv[VEC / 2], wv[VEC / 2];
+                        widen16<T>(xp[u][k], sv);
+                        if constexpr (RESID) {
+                            f32x2 rv[VEC / 2];
+                            widen16<T>(rp[u][k], rv);
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                            for (int q = 0; q < VEC / 2; ++q) sv[q] = f2_add(sv[q], rv[q]);
+                        }
+                        widen16<T>(wp[k], wv);
+#pragma unroll
+                        for (int q = 0; q < VEC / 2; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
+                        st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(sv));
+                    } else {
+                        float v = to_f32(xp[u][k].v[0]);
+                        if constexpr (RESID) v += to_f32(rp[u][k].v[0]);
+                        y[base + c] = from_f32<T>((v * rrms) * to_f32(wp[k].v[0]));
                     }
-                    unpack(wp[k], wv);
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
-                    st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
                 }
             }
         }
