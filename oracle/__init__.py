@@ -66,7 +66,9 @@ def _load():
             lib.orc_encode.argtypes = [i32, p, p, i64]
             lib.orc_rmsnorm_fwd.argtypes = [i32, p, p, p, i64, i64, i64, d, p, p, p, i32]
             lib.orc_rmsnorm_bwd.argtypes = [i32, p, p, p, i64, i64, i64, d, p, p, p, p, p, i32]
-            for f in (lib.orc_decode, lib.orc_encode, lib.orc_rmsnorm_fwd, lib.orc_rmsnorm_bwd):
+            lib.orc_rmsnorm_bwd_residual.argtypes = [i32, p, p, p, p, i64, i64, i64, d, p, p, p, p, p, i32]
+            for f in (lib.orc_decode, lib.orc_encode, lib.orc_rmsnorm_fwd, lib.orc_rmsnorm_bwd,
+                      lib.orc_rmsnorm_bwd_residual):
                 f.restype = i32
             _lib = lib
     return _lib
@@ -157,8 +159,12 @@ def rmsnorm_fwd(x, w, eps: float, dtype: str, residual=None, nthreads: int | Non
 
 
 def rmsnorm_bwd(dy, x, w, eps: float, dtype: str, want_dx: bool = True,
-                want_dweight: bool = True, nthreads: int | None = None):
+                want_dweight: bool = True, nthreads: int | None = None, dres=None):
     """Backward on storage arrays; rrms is recomputed in binary64 from x.
+
+    ``dres`` (M, H storage, optional): the gradient arriving through the
+    fused forward's residual_out; it is added to dx (backward of the fused
+    forward, x = residual_out).
 
     Returns dict: ``dx`` and ``dx_scale`` (M, H) or None, ``dweight`` and
     ``dweight_abs`` (H,) or None, ``rrms`` (M,).  ``dx_scale`` is the size of
@@ -170,9 +176,14 @@ def rmsnorm_bwd(dy, x, w, eps: float, dtype: str, want_dx: bool = True,
     dy, Md, Hd, sd = _matrix(dy, dtype, "dy")
     if (Md, Hd) != (M, H):
         raise ValueError("dy shape differs from x")
-    if sd != stride:
+    if dres is not None:
+        dres, Mr, Hr, sr = _matrix(dres, dtype, "dres")
+        if (Mr, Hr) != (M, H):
+            raise ValueError("dres shape differs from x")
+    if sd != stride or (dres is not None and sr != stride):
         x = np.ascontiguousarray(x)
         dy = np.ascontiguousarray(dy)
+        dres = None if dres is None else np.ascontiguousarray(dres)
         stride = H
     if w is not None:
         w = np.ascontiguousarray(w)
@@ -184,9 +195,15 @@ def rmsnorm_bwd(dy, x, w, eps: float, dtype: str, want_dx: bool = True,
     dweight = np.empty((H,), np.float64) if want_dweight else None
     dweight_abs = np.empty((H,), np.float64) if want_dweight else None
     rrms = np.empty((M,), np.float64)
-    rc = _load().orc_rmsnorm_bwd(DTYPES[dtype], _ptr(dy), _ptr(x), _ptr(w), M, H, stride,
-                                 eps_as_f32(eps), _ptr(dx), _ptr(dx_scale), _ptr(dweight),
-                                 _ptr(dweight_abs), _ptr(rrms), nthreads or default_threads())
+    if dres is None:
+        rc = _load().orc_rmsnorm_bwd(DTYPES[dtype], _ptr(dy), _ptr(x), _ptr(w), M, H, stride,
+                                     eps_as_f32(eps), _ptr(dx), _ptr(dx_scale), _ptr(dweight),
+                                     _ptr(dweight_abs), _ptr(rrms), nthreads or default_threads())
+    else:
+        rc = _load().orc_rmsnorm_bwd_residual(DTYPES[dtype], _ptr(dy), _ptr(dres), _ptr(x), _ptr(w), M, H,
+                                              stride, eps_as_f32(eps), _ptr(dx), _ptr(dx_scale),
+                                              _ptr(dweight), _ptr(dweight_abs), _ptr(rrms),
+                                              nthreads or default_threads())
     if rc:
         raise ValueError(f"orc_rmsnorm_bwd failed ({rc})")
     return {"dx": dx, "dx_scale": dx_scale, "dweight": dweight, "dweight_abs": dweight_abs, "rrms": rrms}

@@ -14,6 +14,9 @@
  *   - Required reasoning 10:   the saved per-row statistic is rrms (reciprocal)
  *   - Required reasoning 12:   dx = rrms*(dy*w) - (xhat*rrms/H) * sum_h(dy*w*xhat),
  *                              xhat = x*rrms;  dweight = sum over rows of dy*xhat
+ *   - Use this when, third bullet (the post-add sum is written back as the
+ *     next block's residual stream): its gradient adds to ds in the backward
+ *     of the fused forward (orc_rmsnorm_bwd_residual)
  * and the PyTorch one-liner printed on the "Rocm Kernels" page
  * (skillselion.com huggingface/kernels/rocm-kernels, "Compare with PyTorch
  * reference"), which states the same forward.
@@ -295,7 +298,7 @@ int orc_rmsnorm_fwd(int dtype, const void *x, const void *r, const void *w,
 
 struct bwd_ctx {
     int dtype;
-    const void *dy, *x, *w;
+    const void *dy, *dres, *x, *w;
     int64_t M, H, stride;
     double eps;
     double *dx, *dx_scale, *dweight, *dweight_abs, *rrms;
@@ -342,6 +345,12 @@ static void bwd_dx_rows(void *p, int64_t i0, int64_t i1)
             c->dx[i * H + h] = rrms * g - xhat * (rrms / (double)H) * dot;
             if (c->dx_scale)
                 c->dx_scale[i * H + h] = fabs(rrms * g) + fabs(xhat * (rrms / (double)H)) * dot_abs;
+            if (c->dres) {   /* gradient arriving through residual_out adds to ds */
+                const double d = load_elem(c->dtype, c->dres, row + h);
+                c->dx[i * H + h] += d;
+                if (c->dx_scale)
+                    c->dx_scale[i * H + h] += fabs(d);
+            }
         }
     }
 }
@@ -384,10 +393,42 @@ static void bwd_dweight_cols(void *p, int64_t h0, int64_t h1)
  * binary64 (recomputed from x; scratch is allocated here if the caller passes
  * NULL).
  */
+static int bwd_common(int dtype, const void *dy, const void *dres, const void *x, const void *w,
+                      int64_t M, int64_t H, int64_t stride, double eps,
+                      double *dx, double *dx_scale, double *dweight, double *dweight_abs,
+                      double *rrms, int nthreads);
+
 int orc_rmsnorm_bwd(int dtype, const void *dy, const void *x, const void *w,
                     int64_t M, int64_t H, int64_t stride, double eps,
                     double *dx, double *dx_scale, double *dweight, double *dweight_abs,
                     double *rrms, int nthreads)
+{
+    return bwd_common(dtype, dy, NULL, x, w, M, H, stride, eps, dx, dx_scale, dweight, dweight_abs, rrms,
+                      nthreads);
+}
+
+/*
+ * Backward of the residual-fused forward (s = x + residual feeds both the
+ * norm and residual_out): ds = (the norm's dx for dy) + dres, where dres is
+ * the gradient arriving through residual_out; ds is the gradient of x and
+ * of residual alike.  x here is the stored residual_out; dweight as for
+ * orc_rmsnorm_bwd (dres does not reach the weight).
+ */
+int orc_rmsnorm_bwd_residual(int dtype, const void *dy, const void *dres, const void *x, const void *w,
+                             int64_t M, int64_t H, int64_t stride, double eps,
+                             double *dx, double *dx_scale, double *dweight, double *dweight_abs,
+                             double *rrms, int nthreads)
+{
+    if (!dres)
+        return 1;
+    return bwd_common(dtype, dy, dres, x, w, M, H, stride, eps, dx, dx_scale, dweight, dweight_abs, rrms,
+                      nthreads);
+}
+
+static int bwd_common(int dtype, const void *dy, const void *dres, const void *x, const void *w,
+                      int64_t M, int64_t H, int64_t stride, double eps,
+                      double *dx, double *dx_scale, double *dweight, double *dweight_abs,
+                      double *rrms, int nthreads)
 {
     if (!elem_size(dtype) || !dy || !x || M < 0 || H <= 0 || stride < H)
         return 1;
@@ -397,7 +438,7 @@ int orc_rmsnorm_bwd(int dtype, const void *dy, const void *x, const void *w,
         if (!rr)
             return 2;
     }
-    struct bwd_ctx c = {dtype, dy, x, w, M, H, stride, eps, dx, dx_scale, dweight, dweight_abs, rr};
+    struct bwd_ctx c = {dtype, dy, dres, x, w, M, H, stride, eps, dx, dx_scale, dweight, dweight_abs, rr};
     parallel_ranges(bwd_rrms_rows, &c, M, nthreads);
     if (dx)
         parallel_ranges(bwd_dx_rows, &c, M, nthreads);

@@ -275,3 +275,36 @@ def test_dx_scale_bounds_dx_and_single_column_form(oracle):
     np.testing.assert_allclose(out["dx"][:, 0], rrms * g * e / (x[:, 0] ** 2 + e), rtol=1e-9)
     big = oracle.rmsnorm_bwd(rng.standard_normal((5, 40)), rng.standard_normal((5, 40)), None, eps, "f64")
     assert np.all(big["dx_scale"] >= np.abs(big["dx"]))
+
+
+def _loss_fused(oracle, x, r, w, dy, dres, eps):
+    """L = sum(dy * y) + sum(dres * s) for the fused forward s = x + r, y = norm(s) * w."""
+    out = oracle.rmsnorm_fwd(_f64(x), _f64(w), eps, "f64", residual=_f64(r))
+    return float(np.sum(dy * out["y"]) + np.sum(dres * out["s"]))
+
+
+@pytest.mark.parametrize("M,H", [(3, 7), (2, 1), (4, 33)])
+def test_fused_backward_central_differences(oracle, M, H):
+    """The fused forward's backward: d/dx and d/dresidual of sum(dy*y) + sum(dres*residual_out)
+    both equal the norm's dx plus dres."""
+    rng = np.random.default_rng(200 + M * H)
+    x, r = rng.standard_normal((M, H)), rng.standard_normal((M, H))
+    w = 1 + 0.3 * rng.standard_normal(H)
+    dy, dres = rng.standard_normal((M, H)), rng.standard_normal((M, H))
+    eps = 1e-3
+    out = oracle.rmsnorm_bwd(dy, x + r, w, eps, "f64", dres=dres)
+    h = 1e-6
+    for which in ("x", "r"):
+        fd = np.zeros((M, H))
+        for i in range(M):
+            for k in range(H):
+                a, b = [x.copy(), r.copy()], [x.copy(), r.copy()]
+                j = 0 if which == "x" else 1
+                a[j][i, k] += h
+                b[j][i, k] -= h
+                fd[i, k] = (_loss_fused(oracle, a[0], a[1], w, dy, dres, eps)
+                            - _loss_fused(oracle, b[0], b[1], w, dy, dres, eps)) / (2 * h)
+        np.testing.assert_allclose(out["dx"], fd, rtol=1e-6, atol=1e-8)
+    plain = oracle.rmsnorm_bwd(dy, x + r, w, eps, "f64")
+    np.testing.assert_allclose(out["dweight"], plain["dweight"], rtol=0, atol=0)   # dres does not reach w
+    assert np.all(out["dx_scale"] >= np.abs(out["dx"]))
