@@ -2,7 +2,8 @@
 """Benchmark of the GB300 RMSNorm engine.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                    [--workload step|fused_fwd|dit_mix|fwd_bwd_8192|fused_f16_padded]
+                    [--workload step|fused_fwd|fused_fwd_bwd_residual|dit_mix|fwd_f32_small|
+                                fwd_bwd_8192|fused_f16_padded]
 
 Default workload ("step"): one pass of the whole hot path on the
 (B=8, T=2048, H=4096) bf16 activations, M = 16384 rows -- the fused
@@ -165,11 +166,12 @@ def summarize_clocks(rows, t0, t1):
 # workloads
 # --------------------------------------------------------------------------
 
-def step_bytes(M, H, es, fused=True, weight=True, save_rrms=True, backward=True):
-    """Algorithmic bytes: each M x H tensor once, plus weight, rrms, dweight."""
+def step_bytes(M, H, es, fused=True, weight=True, save_rrms=True, backward=True, dres=False):
+    """Algorithmic bytes: each M x H tensor once, plus weight, rrms, dweight
+    (the fused backward also reads the residual stream's gradient)."""
     mh = M * H * es
     fwd = (4 if fused else 2) * mh + (H * es if weight else 0) + (M * 4 if save_rrms else 0)
-    bwd = (3 * mh + M * 4 + (H * es + H * 4 if weight else 0)) if backward else 0
+    bwd = ((4 if dres else 3) * mh + M * 4 + (H * es + H * 4 if weight else 0)) if backward else 0
     return fwd, bwd
 
 
@@ -179,7 +181,7 @@ class StepWorkload:
 
     flush_l2 = False
 
-    def __init__(self, cfg_id=2, backward=True, fused=None):
+    def __init__(self, cfg_id=2, backward=True, fused=None, dres=False):
         import torch
         import residual_add_rmsnorm_fwd_gb300 as rn
         import workloads as wl
@@ -190,10 +192,16 @@ class StepWorkload:
         self.backward = backward
         self.M, self.H, self.S, self.dt = c["M"], c["H"], c["stride"], c["dtype"]
         self.es = wl.ELEM_BYTES[self.dt]
-        self.fwd_bytes, self.bwd_bytes = step_bytes(self.M, self.H, self.es, self.fused, True, backward, backward)
+        self.dres = dres and self.fused and backward
+        self.fwd_bytes, self.bwd_bytes = step_bytes(self.M, self.H, self.es, self.fused, True, backward, backward,
+                                                    self.dres)
         self.bytes_per_step = self.fwd_bytes + self.bwd_bytes
         self.rows_per_step = self.M
         self.host = wl.generate(cfg_id, with_dy=backward)
+        if self.dres:   # the residual stream's incoming gradient, drawn after dy
+            rng = wl.rng_for(self.c["seed"] + 100)
+            self.host["dres"] = wl.matrix(rng, self.M, self.H, self.dt, self.S)
+            self.name = "fused_fwd_bwd_residual_bf16_B8xT2048xH4096" if cfg_id == 2 else self.name
         self.kernels_per_step = 1 + (2 if backward else 0)
 
     def _make_set(self):
@@ -218,6 +226,7 @@ class StepWorkload:
         b.rrms = torch.empty(M, device=dev) if self.backward else None
         if self.backward:
             b.dy = up(self.host["dy"])
+            b.dres = up(self.host["dres"]) if self.dres else None
             b.dx = out()
             b.dw = torch.empty(H, device=dev)
             b.ws = torch.empty(max(1, self.rn.rmsnorm_bwd_workspace_bytes(M, H, tdt)), dtype=torch.uint8,
@@ -238,7 +247,10 @@ class StepWorkload:
                         self.fwd_bytes))
         else:
             out.append(("fwd", lambda: rn.rmsnorm_fwd(b.x, self.w, b.y, b.rrms, eps=eps), self.fwd_bytes))
-        if self.backward:
+        if self.dres:
+            out.append(("bwd_residual", lambda: rn.rmsnorm_bwd_residual(b.dy, b.dres, b.s, self.w, b.rrms, b.dx, b.dw,
+                                                                        b.ws), self.bwd_bytes))
+        elif self.backward:
             xin = b.s if self.fused else b.x
             out.append(("bwd", lambda: rn.rmsnorm_bwd(b.dy, xin, self.w, b.rrms, b.dx, b.dw, b.ws), self.bwd_bytes))
         return out
@@ -260,7 +272,7 @@ class StepWorkload:
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
         host = lambda a: self.wl.to_torch(a, self.dt)[:, :self.H].contiguous().pin_memory()  # noqa: E731
         self.h_in = [host(self.host["x"])] + ([host(self.host["residual"])] if self.fused else []) + \
-            ([host(self.host["dy"])] if self.backward else [])
+            ([host(self.host["dy"])] if self.backward else []) + ([host(self.host["dres"])] if self.dres else [])
         outs = [b.y] + ([b.s] if self.fused else []) + ([b.dx, b.dw] if self.backward else [])
         self.h_out = [pin(t) for t in outs]
         while len(self.sets) < 2:
@@ -271,7 +283,8 @@ class StepWorkload:
     def e2e_transfers(self, k):
         """([(device, host)] inputs, [(host, device)] results) of buffer set k."""
         b = self.sets[k]
-        dev_in = [b.x] + ([b.r] if self.fused else []) + ([b.dy] if self.backward else [])
+        dev_in = [b.x] + ([b.r] if self.fused else []) + ([b.dy] if self.backward else []) + \
+            ([b.dres] if self.dres else [])
         dev_out = [b.y] + ([b.s] if self.fused else []) + ([b.dx, b.dw] if self.backward else [])
         return list(zip(dev_in, self.h_in)), list(zip(self.h_out, dev_out))
 
@@ -284,7 +297,8 @@ class StepWorkload:
         f = oracle.rmsnorm_fwd(x, self.host["w"], eps, dt, residual=r)
         if self.backward:
             s = oracle.encode(f["s"], dt)
-            oracle.rmsnorm_bwd(self.host["dy"][:rows, :H], s, self.host["w"], eps, dt)
+            oracle.rmsnorm_bwd(self.host["dy"][:rows, :H], s, self.host["w"], eps, dt,
+                               dres=self.host["dres"][:rows, :H] if self.dres else None)
         return rows * self.bytes_per_step / self.M
 
 
@@ -393,6 +407,7 @@ WORKLOADS = {
     "dit_mix": DitMixWorkload,
     "step": lambda: StepWorkload(2, backward=True),
     "fused_fwd": lambda: StepWorkload(2, backward=False),
+    "fused_fwd_bwd_residual": lambda: StepWorkload(2, backward=True, dres=True),
     "fwd_bwd_8192": lambda: StepWorkload(4, backward=True),
     "fused_f16_padded": lambda: StepWorkload(5, backward=True),
 }

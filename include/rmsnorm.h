@@ -102,8 +102,9 @@ int rmsnorm_fwd_residual(const void *x, const void *residual, const void *weight
                          int dtype, int has_weight, void *stream);
 
 /*
- * Size in bytes of the workspace rmsnorm_bwd needs for (M, H, dtype) on the
- * current device (per-CTA binary32 dweight partials).  Writes *bytes; the
+ * Size in bytes of the workspace rmsnorm_bwd (and rmsnorm_bwd_residual)
+ * needs for (M, H, dtype) on the current device (per-CTA binary32 dweight
+ * partials).  Writes *bytes; the
  * value is fixed for a given device, M, H and dtype.  0 means no workspace
  * is needed.
  */
@@ -133,6 +134,28 @@ int rmsnorm_bwd(const void *dy, const void *x, const void *weight, const float *
                 void *dx, float *dweight, void *workspace, size_t workspace_bytes,
                 int64_t row_stride, int64_t M, int64_t H,
                 int dtype, int has_weight, void *stream);
+
+/*
+ * Backward of rmsnorm_fwd_residual when residual_out also feeds later
+ * layers.  (The RMSNorm skill page, Use this when, third bullet: the
+ * post-add sum is written back as the next block's residual stream; the
+ * pages leave its backward implicit.)  s = x + residual feeds both y and
+ * residual_out, so
+ *   ds = (rmsnorm_bwd's dx for dy) + dresidual_out,
+ * computed in the same pass (one read of dresidual_out instead of a separate
+ * add kernel); ds is the gradient of x and of residual alike.
+ *   dy             in   M x H, row_stride: gradient of y
+ *   dresidual_out  in   M x H, row_stride: gradient arriving through residual_out
+ *   x              in   M x H, row_stride: the forward's residual_out
+ *   weight, rrms, dweight, workspace: as for rmsnorm_bwd (dresidual_out does
+ *   not reach dweight); the workspace size from rmsnorm_bwd_workspace_bytes
+ *   covers this call too.
+ *   dx             out  M x H, row_stride: ds
+ */
+int rmsnorm_bwd_residual(const void *dy, const void *dresidual_out, const void *x, const void *weight,
+                         const float *rrms, void *dx, float *dweight, void *workspace,
+                         size_t workspace_bytes, int64_t row_stride, int64_t M, int64_t H,
+                         int dtype, int has_weight, void *stream);
 
 /*
  * Backward for callers that cannot allocate device memory.  No counterpart

@@ -23,7 +23,8 @@ import threading
 __all__ = [
     "RMSN_F32", "RMSN_F16", "RMSN_BF16", "RmsnormError", "lib", "lib_path",
     "rmsnorm_fwd", "rmsnorm_fwd_residual", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
-    "rmsnorm_bwd_noalloc", "rmsnorm_read_device_errors", "rmsnorm_status_string", "dtype_code",
+    "rmsnorm_bwd_residual", "rmsnorm_bwd_noalloc", "rmsnorm_read_device_errors", "rmsnorm_status_string",
+    "dtype_code",
 ]
 
 RMSN_F32, RMSN_F16, RMSN_BF16 = 0, 1, 2
@@ -62,6 +63,8 @@ def lib():
             L.rmsnorm_fwd_residual.argtypes = [p, p, p, p, p, p, i64, i64, i64, f32, i32, i32, p]
             L.rmsnorm_bwd_workspace_bytes.argtypes = [i64, i64, i32, ctypes.POINTER(sz)]
             L.rmsnorm_bwd.argtypes = [p, p, p, p, p, p, p, sz, i64, i64, i64, i32, i32, p]
+            L.rmsnorm_bwd_residual.argtypes = [p, p, p, p, p, p, p, p, sz, i64, i64, i64, i32, i32, p]
+            L.rmsnorm_bwd_residual.restype = i32
             L.rmsnorm_bwd_noalloc.argtypes = [p, p, p, p, p, p, i64, i64, i64, i32, i32, p]
             L.rmsnorm_bwd_noalloc.restype = i32
             L.rmsnorm_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint)]
@@ -151,6 +154,16 @@ def rmsnorm_bwd_workspace_bytes(M: int, H: int, dtype) -> int:
     out = ctypes.c_size_t(0)
     _check("rmsnorm_bwd_workspace_bytes", lib().rmsnorm_bwd_workspace_bytes(M, H, code, ctypes.byref(out)))
     return out.value
+
+
+def rmsnorm_bwd_residual(dy, dresidual_out, x, weight, rrms, dx, dweight=None, workspace=None, stream=None):
+    """Backward of the residual-fused forward: dx = norm backward + dresidual_out
+    (x is the forward's residual_out; dx is the gradient of x and residual)."""
+    M, H, stride = _shared_stride([(dy, "dy"), (dresidual_out, "dresidual_out"), (x, "x"), (dx, "dx")])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("rmsnorm_bwd_residual", lib().rmsnorm_bwd_residual(
+        _ptr(dy), _ptr(dresidual_out), _ptr(x), _ptr(weight), _ptr(rrms), _ptr(dx), _ptr(dweight),
+        _ptr(workspace), ws_bytes, stride, M, H, dtype_code(x.dtype), int(weight is not None), _stream(stream)))
 
 
 def rmsnorm_bwd_noalloc(dy, x, weight, rrms, dx, dweight=None, stream=None):

@@ -228,7 +228,7 @@ bool fwd_ring_geometry(int H, int dtype, bool resid, RingPlan *p) {
 // pipe, and the longer per-thread chains measured faster: H = 6144 f16, 205
 // against 245 us).  Two stages, as many CTAs per SM as fit -- the backward
 // profits from every resident warp.  Measured on GB300 at H = 4096-8192.
-bool bwd_ring_geometry(int H, int dtype, RingPlan *p) {
+bool bwd_ring_geometry(int H, int dtype, bool dres, RingPlan *p) {
     const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
     if (row_bytes % 16 != 0 || row_bytes < 2048) return false;
     const int nvec = (int)(row_bytes / 16);
@@ -236,9 +236,10 @@ bool bwd_ring_geometry(int H, int dtype, RingPlan *p) {
     const int threads = round_up_to(ceil_div(nvec, nv), 32);
     if (threads > 512) return false;
     const int stages = 2;
-    const size_t smem = kRingHeaderBytes + (size_t)stages * 2 * round_up_to((int)row_bytes, 128);
+    const int streams = dres ? 3 : 2;
+    const size_t smem = kRingHeaderBytes + (size_t)stages * streams * round_up_to((int)row_bytes, 128);
     if (smem > 200 * 1024) return false;
-    finish_ring(p, nv, threads, row_bytes, 2, stages, 0);
+    finish_ring(p, nv, threads, row_bytes, streams, stages, 0);
     return true;
 }
 
@@ -257,6 +258,76 @@ int occupancy(const void *func, int threads, size_t smem) {
     g_occ[key] = n;
     return n;
 }
+
+namespace {
+
+int backward(const void *dy, const void *dres, const void *x, const void *weight, const float *rrms, void *dx,
+             float *dweight, void *workspace, size_t workspace_bytes, int64_t row_stride, int64_t M, int64_t H,
+             int dtype, int has_weight, void *stream, bool fused) {
+    int st = check_shape(M, H, row_stride, dtype);
+    if (st) return st;
+    if (has_weight && weight == nullptr) return RMSN_ERR_INVALID;
+    if (M > 0 && (dy == nullptr || x == nullptr || rrms == nullptr || dx == nullptr || (fused && dres == nullptr)))
+        return RMSN_ERR_INVALID;  // with no rows the row pointers are never used
+    const int es = elem_bytes(dtype);
+    const void *w = has_weight ? weight : nullptr;
+    float *dw = has_weight ? dweight : nullptr;
+    const void *dr = fused ? dres : nullptr;
+    for (const void *p : {dy, dr, x, w, static_cast<const void *>(dx)})
+        if (p != nullptr && !aligned(p, es)) return RMSN_ERR_INVALID;
+    if ((rrms != nullptr && !aligned(rrms, 4)) || (dw != nullptr && !aligned(dw, 4))) return RMSN_ERR_INVALID;
+
+    if (M == 0) {
+        // no rows: dweight is an empty sum
+        if (dw != nullptr) return to_status(cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float),
+                                                            static_cast<cudaStream_t>(stream)));
+        return RMSN_OK;
+    }
+    int dev = 0, sms = 0;
+    st = current_device(&dev, &sms);
+    if (st) return st;
+
+    bool vec = rows_vectorisable(H, row_stride, dtype);
+    for (const void *p : {dy, dr, x, w, static_cast<const void *>(dx)})
+        if (p != nullptr && !aligned(p, 16)) vec = false;
+    const BwdPlan plan = plan_bwd(M, (int)H, dtype, vec, fused, sms);
+    const size_t part_bytes = dw != nullptr ? bwd_partial_bytes(plan, (int)H) : 0;
+    if (dw != nullptr) {
+        if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < part_bytes)
+            return RMSN_ERR_WORKSPACE;
+    }
+
+    const Range rdy = matrix_of(dy, M, H, row_stride, es);
+    const Range rx = matrix_of(x, M, H, row_stride, es);
+    const Range rw = bytes_of(w, (size_t)H * es);
+    const Range rq = bytes_of(rrms, (size_t)M * sizeof(float));
+    const Range rdr = matrix_of(dr, M, H, row_stride, es);
+    const Range rdx = matrix_of(dx, M, H, row_stride, es);
+    const Range rdw = bytes_of(dw, (size_t)H * sizeof(float));
+    const Range rws = bytes_of(dw != nullptr ? workspace : nullptr, part_bytes);
+    const Range outs[] = {rdx, rdw, rws};
+    const Range all[] = {rdy, rx, rw, rq, rdr, rdx, rdw, rws};
+    for (int o = 0; o < 3; ++o)
+        for (int k = 0; k < 8; ++k)
+            if (k != 5 + o && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
+
+    BwdArgs a{};
+    a.err = device_error_word(dev);
+    a.dy = dy;
+    a.dres = dr;
+    a.x = x;
+    a.w = w;
+    a.rrms = rrms;
+    a.dx = dx;
+    a.partial = dw != nullptr ? static_cast<float *>(workspace) : nullptr;
+    a.stride = row_stride;
+    a.M = M;
+    a.H = (int)H;
+    a.has_w = has_weight ? 1 : 0;
+    return to_status(launch_bwd(a, plan, dtype, vec, dw, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
 
 }  // namespace rmsn
 
@@ -288,77 +359,32 @@ RMSN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype, size_t
     int dev = 0, sms = 0;
     st = current_device(&dev, &sms);
     if (st) return st;
-    // the largest of the variants rmsnorm_bwd may pick for this shape
-    size_t need = bwd_partial_bytes(plan_bwd(M, (int)H, dtype, false, sms), (int)H);
-    if ((H * elem_bytes(dtype)) % 16 == 0) {
-        const size_t v = bwd_partial_bytes(plan_bwd(M, (int)H, dtype, true, sms), (int)H);
-        need = v > need ? v : need;
+    // the largest of the variants rmsnorm_bwd and rmsnorm_bwd_residual may pick
+    size_t need = 0;
+    for (int vec = 0; vec < 2; ++vec) {
+        if (vec && (H * elem_bytes(dtype)) % 16 != 0) continue;
+        for (int dres = 0; dres < 2; ++dres) {
+            const size_t v = bwd_partial_bytes(plan_bwd(M, (int)H, dtype, vec != 0, dres != 0, sms), (int)H);
+            need = v > need ? v : need;
+        }
     }
     *bytes = need;
     return RMSN_OK;
 }
 
 RMSN_API int rmsnorm_bwd(const void *dy, const void *x, const void *weight, const float *rrms, void *dx, float *dweight,
-                void *workspace, size_t workspace_bytes, int64_t row_stride, int64_t M, int64_t H, int dtype,
-                int has_weight, void *stream) {
-    int st = check_shape(M, H, row_stride, dtype);
-    if (st) return st;
-    if (has_weight && weight == nullptr) return RMSN_ERR_INVALID;
-    if (M > 0 && (dy == nullptr || x == nullptr || rrms == nullptr || dx == nullptr))
-        return RMSN_ERR_INVALID;  // with no rows the row pointers are never used
-    const int es = elem_bytes(dtype);
-    const void *w = has_weight ? weight : nullptr;
-    float *dw = has_weight ? dweight : nullptr;
-    for (const void *p : {dy, x, w, static_cast<const void *>(dx)})
-        if (p != nullptr && !aligned(p, es)) return RMSN_ERR_INVALID;
-    if ((rrms != nullptr && !aligned(rrms, 4)) || (dw != nullptr && !aligned(dw, 4))) return RMSN_ERR_INVALID;
+                         void *workspace, size_t workspace_bytes, int64_t row_stride, int64_t M, int64_t H, int dtype,
+                         int has_weight, void *stream) {
+    return backward(dy, nullptr, x, weight, rrms, dx, dweight, workspace, workspace_bytes, row_stride, M, H, dtype,
+                    has_weight, stream, false);
+}
 
-    if (M == 0) {
-        // no rows: dweight is an empty sum
-        if (dw != nullptr) return to_status(cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float),
-                                                            static_cast<cudaStream_t>(stream)));
-        return RMSN_OK;
-    }
-    int dev = 0, sms = 0;
-    st = current_device(&dev, &sms);
-    if (st) return st;
-
-    bool vec = rows_vectorisable(H, row_stride, dtype);
-    for (const void *p : {dy, x, w, static_cast<const void *>(dx)})
-        if (p != nullptr && !aligned(p, 16)) vec = false;
-    const BwdPlan plan = plan_bwd(M, (int)H, dtype, vec, sms);
-    const size_t part_bytes = dw != nullptr ? bwd_partial_bytes(plan, (int)H) : 0;
-    if (dw != nullptr) {
-        if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < part_bytes)
-            return RMSN_ERR_WORKSPACE;
-    }
-
-    const Range rdy = matrix_of(dy, M, H, row_stride, es);
-    const Range rx = matrix_of(x, M, H, row_stride, es);
-    const Range rw = bytes_of(w, (size_t)H * es);
-    const Range rq = bytes_of(rrms, (size_t)M * sizeof(float));
-    const Range rdx = matrix_of(dx, M, H, row_stride, es);
-    const Range rdw = bytes_of(dw, (size_t)H * sizeof(float));
-    const Range rws = bytes_of(dw != nullptr ? workspace : nullptr, part_bytes);
-    const Range outs[] = {rdx, rdw, rws};
-    const Range all[] = {rdy, rx, rw, rq, rdx, rdw, rws};
-    for (int o = 0; o < 3; ++o)
-        for (int k = 0; k < 7; ++k)
-            if (k != 4 + o && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
-
-    BwdArgs a{};
-    a.err = device_error_word(dev);
-    a.dy = dy;
-    a.x = x;
-    a.w = w;
-    a.rrms = rrms;
-    a.dx = dx;
-    a.partial = dw != nullptr ? static_cast<float *>(workspace) : nullptr;
-    a.stride = row_stride;
-    a.M = M;
-    a.H = (int)H;
-    a.has_w = has_weight ? 1 : 0;
-    return to_status(launch_bwd(a, plan, dtype, vec, dw, static_cast<cudaStream_t>(stream)));
+RMSN_API int rmsnorm_bwd_residual(const void *dy, const void *dresidual_out, const void *x, const void *weight,
+                                  const float *rrms, void *dx, float *dweight, void *workspace,
+                                  size_t workspace_bytes, int64_t row_stride, int64_t M, int64_t H, int dtype,
+                                  int has_weight, void *stream) {
+    return backward(dy, dresidual_out, x, weight, rrms, dx, dweight, workspace, workspace_bytes, row_stride, M, H,
+                    dtype, has_weight, stream, true);
 }
 
 RMSN_API int rmsnorm_read_device_errors(unsigned *flags) {

@@ -21,11 +21,12 @@ namespace rmsn {
 
 // Row kept in registers: a thread owns NV groups of VEC columns; its
 // dweight partials for those columns stay in registers across all its rows.
-template <typename T, int VEC, int NV>
+template <typename T, int VEC, int NV, bool DRES>
 __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
     using P = Pack<T, VEC>;
     __shared__ float red[64];
     const T *__restrict__ dy = static_cast<const T *>(a.dy);
+    const T *__restrict__ dres = static_cast<const T *>(a.dres);
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ w = static_cast<const T *>(a.w);
     T *__restrict__ dx = static_cast<T *>(a.dx);
@@ -46,13 +47,14 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * a.stride;
         const float rr = __ldg(a.rrms + row);
-        P gp[NV], xp[NV];
+        P gp[NV], xp[NV], rp[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
                 gp[i] = ld_stream<T, VEC>(dy + base + (int64_t)c * VEC);
                 xp[i] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
+                if constexpr (DRES) rp[i] = ld_stream<T, VEC>(dres + base + (int64_t)c * VEC);
             }
         }
         float dot = 0.0f;
@@ -84,6 +86,12 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
                 unpack(wp[i], wv);
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) d[j] = rr * (d[j] * wv[j] - (xv[j] * rr) * c_row);
+                if constexpr (DRES) {   // the residual stream's gradient joins ds
+                    float rv[VEC];
+                    unpack(rp[i], rv);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) d[j] += rv[j];
+                }
                 st_global<T, VEC>(dx + base + (int64_t)c * VEC, pack<T, VEC>(d));
             }
         }
@@ -113,12 +121,13 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
 // bounds.  The CTA's dweight partial row lives in the workspace; it belongs
 // to this CTA alone, so it is updated with plain read-modify-write (the
 // first row of the CTA initialises it).
-template <typename T, int VEC>
+template <typename T, int VEC, bool DRES>
 __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
     using P = Pack<T, VEC>;
     constexpr int U = 2;
     __shared__ float red[64];
     const T *__restrict__ dy = static_cast<const T *>(a.dy);
+    const T *__restrict__ dres = static_cast<const T *>(a.dres);
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ w = static_cast<const T *>(a.w);
     T *__restrict__ dx = static_cast<T *>(a.dx);
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
         const float c_row = block_sum(dot, red, bank) / hf;
         bank ^= 1;
         for (int c0 = 0; c0 < nvec; c0 += chunk) {
-            P gp[U], xp[U], wp[U];
+            P gp[U], xp[U], wp[U], rp[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * blockDim.x + threadIdx.x;
@@ -168,20 +177,23 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
                     gp[u] = ld_stream<T, VEC>(dy + base + (int64_t)c * VEC);
                     xp[u] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
                     wp[u] = a.has_w ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+                    if constexpr (DRES) rp[u] = ld_stream<T, VEC>(dres + base + (int64_t)c * VEC);
                 }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * blockDim.x + threadIdx.x;
                 if (c < nvec) {
-                    float d[VEC], xv[VEC], wv[VEC], o[VEC];
+                    float d[VEC], xv[VEC], wv[VEC], o[VEC], rv[VEC];
                     unpack(gp[u], d);
                     unpack(xp[u], xv);
                     unpack(wp[u], wv);
+                    if constexpr (DRES) unpack(rp[u], rv);
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
                         const float xh = xv[j] * rr;
                         o[j] = rr * (d[j] * wv[j] - xh * c_row);
+                        if constexpr (DRES) o[j] += rv[j];
                         if (prow != nullptr) {
                             float *p = prow + (int64_t)c * VEC + j;
                             *p = first ? d[j] * xh : *p + d[j] * xh;
@@ -252,54 +264,60 @@ bool pick_row(int nvec, bool vec, int &threads, int &nv) {
     return false;
 }
 
-template <typename T, int VEC, int NV>
+template <typename T, int VEC, int NV, bool DRES>
 const void *row_kernel() {
-    return reinterpret_cast<const void *>(bwd_row_kernel<T, VEC, NV>);
+    return reinterpret_cast<const void *>(bwd_row_kernel<T, VEC, NV, DRES>);
 }
 
-template <typename T>
+template <typename T, bool DRES>
 const void *row_kernel_for(bool vec, int nv) {
     constexpr int V = Vec16<T>::n;
     if (vec) {
         switch (nv) {
-        case 1: return row_kernel<T, V, 1>();
-        case 2: return row_kernel<T, V, 2>();
+        case 1: return row_kernel<T, V, 1, DRES>();
+        case 2: return row_kernel<T, V, 2, DRES>();
         }
     } else {
         switch (nv) {
-        case 1: return row_kernel<T, 1, 1>();
-        case 2: return row_kernel<T, 1, 2>();
-        case 4: return row_kernel<T, 1, 4>();
-        case 8: return row_kernel<T, 1, 8>();
+        case 1: return row_kernel<T, 1, 1, DRES>();
+        case 2: return row_kernel<T, 1, 2, DRES>();
+        case 4: return row_kernel<T, 1, 4, DRES>();
+        case 8: return row_kernel<T, 1, 8, DRES>();
         }
     }
     return nullptr;
 }
 
-template <typename T>
+template <typename T, bool DRES>
 const void *chunked_kernel_for(bool vec) {
     constexpr int V = Vec16<T>::n;
-    return vec ? reinterpret_cast<const void *>(bwd_chunked_kernel<T, V>)
-               : reinterpret_cast<const void *>(bwd_chunked_kernel<T, 1>);
+    return vec ? reinterpret_cast<const void *>(bwd_chunked_kernel<T, V, DRES>)
+               : reinterpret_cast<const void *>(bwd_chunked_kernel<T, 1, DRES>);
+}
+
+template <typename T>
+const void *kernel_for_dt(const BwdPlan &p, bool vec) {
+    if (p.dres) return p.kind == kBwdRow ? row_kernel_for<T, true>(vec, p.nv) : chunked_kernel_for<T, true>(vec);
+    return p.kind == kBwdRow ? row_kernel_for<T, false>(vec, p.nv) : chunked_kernel_for<T, false>(vec);
 }
 
 const void *kernel_for(const BwdPlan &p, int dtype, bool vec) {
-    if (p.kind == kBwdRing) return bwd_ring_kernel_for(dtype, p.nv);
-    const bool row = p.kind == kBwdRow;
+    if (p.kind == kBwdRing) return bwd_ring_kernel_for(dtype, p.nv, p.dres);
     switch (dtype) {
-    case kF32: return row ? row_kernel_for<float>(vec, p.nv) : chunked_kernel_for<float>(vec);
-    case kF16: return row ? row_kernel_for<__half>(vec, p.nv) : chunked_kernel_for<__half>(vec);
-    case kBF16: return row ? row_kernel_for<__nv_bfloat16>(vec, p.nv) : chunked_kernel_for<__nv_bfloat16>(vec);
+    case kF32: return kernel_for_dt<float>(p, vec);
+    case kF16: return kernel_for_dt<__half>(p, vec);
+    case kBF16: return kernel_for_dt<__nv_bfloat16>(p, vec);
     }
     return nullptr;
 }
 
 }  // namespace
 
-BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, int sm_count) {
+BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool dres, int sm_count) {
     BwdPlan p{};
+    p.dres = dres;
     RingPlan rp{};
-    if (vec && bwd_ring_geometry(H, dtype, &rp)) {
+    if (vec && bwd_ring_geometry(H, dtype, dres, &rp)) {
         p.kind = kBwdRing;
         p.threads = rp.threads;
         p.nv = rp.nv;

@@ -3,8 +3,10 @@
 //
 // Same arithmetic as the register-resident backward kernel (bwd.cu):
 //     dot  = sum_h (dy_h * w_h) * (x_h * rrms)          (CTA reduction)
-//     dx_h = rrms * (dy_h * w_h - (x_h * rrms) * dot / H)
+//     dx_h = rrms * (dy_h * w_h - (x_h * rrms) * dot / H)  (+ dres_h, DRES)
 //     partial[b][h] += dy_h * (x_h * rrms)               (CTA b's rows)
+// With DRES (the backward of the residual-fused forward) a third row, the
+// gradient arriving through residual_out, is staged and added to dx.
 // but the rows arrive through a ring of NST shared-memory stages kept full by
 // one thread's cp.async.bulk copies (mbarrier byte counts), so the next rows
 // stream in from HBM while the current one is reduced and written.  The
@@ -18,10 +20,11 @@
 
 namespace rmsn {
 
-template <typename T, int NV>
+template <typename T, int NV, bool DRES>
 __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) {
     constexpr int VEC = Vec16<T>::n;
     constexpr int PR = Pairs16<T>::n;
+    constexpr int NS = DRES ? 3 : 2;   // streams staged per row: dy, x (and dres)
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
@@ -29,6 +32,7 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
     unsigned char *stages = smem + kRingHeaderBytes;
 
     const T *__restrict__ dy = static_cast<const T *>(a.dy);
+    const T *__restrict__ dres = static_cast<const T *>(a.dres);
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ w = static_cast<const T *>(a.w);
     T *__restrict__ dx = static_cast<T *>(a.dx);
@@ -38,13 +42,14 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
     const int64_t G = gridDim.x;
     const int64_t nrows = (a.M - 1 - blockIdx.x) / G + 1;  // the grid never exceeds M
 
-    auto stage = [&](int s, int j) { return stages + (size_t)(s * 2 + j) * rs.row_pitch; };
+    auto stage = [&](int s, int j) { return stages + (size_t)(s * NS + j) * rs.row_pitch; };
     auto issue = [&](int64_t k) {
         const int s = (int)(k % nst);
         const int64_t base = (blockIdx.x + k * G) * a.stride;
-        mbar_arrive_expect_tx(&full[s], 2 * rs.row_bytes);
+        mbar_arrive_expect_tx(&full[s], NS * rs.row_bytes);
         bulk_g2s(stage(s, 0), dy + base, rs.row_bytes, &full[s]);
         bulk_g2s(stage(s, 1), x + base, rs.row_bytes, &full[s]);
+        if constexpr (DRES) bulk_g2s(stage(s, 2), dres + base, rs.row_bytes, &full[s]);
     };
 
     if (threadIdx.x == 0) {
@@ -76,7 +81,7 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
         const f32x2 rr2 = f2_make(rr, rr);
         if (!mbar_wait_bounded(&full[s], (uint32_t)((k / nst) & 1), a.err)) gave_up = true;
 
-        P gp[NV], xp[NV];
+        P gp[NV], xp[NV], rp[NV];
         f32x2 dot2 = f2_make(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
@@ -84,6 +89,7 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
             if (c < nvec) {
                 gp[i] = *reinterpret_cast<const P *>(stage(s, 0) + (size_t)c * 16);
                 xp[i] = *reinterpret_cast<const P *>(stage(s, 1) + (size_t)c * 16);
+                if constexpr (DRES) rp[i] = *reinterpret_cast<const P *>(stage(s, 2) + (size_t)c * 16);
                 f32x2 d[PR], xv[PR], wv[PR];
                 widen16<T>(gp[i], d);
                 widen16<T>(xp[i], xv);
@@ -115,6 +121,12 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
 #pragma unroll
                 for (int q = 0; q < PR; ++q)   // rrms * (g - xhat * c)
                     d[q] = f2_mul(rr2, f2_fma(f2_mul(xv[q], rr2), nc2, f2_mul(d[q], wv[q])));
+                if constexpr (DRES) {           // the residual stream's gradient joins ds
+                    f32x2 rv[PR];
+                    widen16<T>(rp[i], rv);
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) d[q] = f2_add(d[q], rv[q]);
+                }
                 st_global<T, VEC>(dx + base + (int64_t)c * VEC, narrow16<T>(d));
             }
         }
@@ -146,24 +158,24 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
 
 namespace {
 
-template <typename T>
+template <typename T, bool DRES>
 const void *kernel_nv(int nv) {
     switch (nv) {
-    case 1: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 1>);
-    case 2: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 2>);
-    case 3: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 3>);
-    case 4: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 4>);
+    case 1: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 1, DRES>);
+    case 2: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 2, DRES>);
+    case 3: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 3, DRES>);
+    case 4: return reinterpret_cast<const void *>(bwd_ring_kernel<T, 4, DRES>);
     }
     return nullptr;
 }
 
 }  // namespace
 
-const void *bwd_ring_kernel_for(int dtype, int nv) {
+const void *bwd_ring_kernel_for(int dtype, int nv, bool dres) {
     switch (dtype) {
-    case kF32: return kernel_nv<float>(nv);
-    case kF16: return kernel_nv<__half>(nv);
-    case kBF16: return kernel_nv<__nv_bfloat16>(nv);
+    case kF32: return dres ? kernel_nv<float, true>(nv) : kernel_nv<float, false>(nv);
+    case kF16: return dres ? kernel_nv<__half, true>(nv) : kernel_nv<__half, false>(nv);
+    case kBF16: return dres ? kernel_nv<__nv_bfloat16, true>(nv) : kernel_nv<__nv_bfloat16, false>(nv);
     }
     return nullptr;
 }

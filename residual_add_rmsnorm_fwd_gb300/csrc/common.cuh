@@ -32,6 +32,7 @@ struct FwdArgs {
 
 struct BwdArgs {
     const void *dy;
+    const void *dres;     // gradient arriving through the fused forward's residual_out, or nullptr
     const void *x;
     const void *w;
     const float *rrms;

@@ -46,7 +46,7 @@ struct RingPlan {
 // Ring shapes measured best on GB300 (see the kernel files): false when the
 // row is too short to profit from the ring or too long for it.
 bool fwd_ring_geometry(int H, int dtype, bool resid, RingPlan *p);
-bool bwd_ring_geometry(int H, int dtype, RingPlan *p);
+bool bwd_ring_geometry(int H, int dtype, bool dres, RingPlan *p);
 
 // Forward with rows staged by bulk copies (16-byte aligned rows only).
 bool plan_fwd_ring(int64_t M, int H, int dtype, bool resid, int sm_count, RingPlan *out);
@@ -67,14 +67,15 @@ cudaError_t launch_fwd_chunked(const FwdArgs &a, int dtype, bool vec, int sm_cou
 enum BwdKind { kBwdRow = 0, kBwdChunked = 1, kBwdRing = 2 };
 struct BwdPlan {
     int kind;        // BwdKind
+    bool dres;       // adds the residual stream's gradient (fused-forward backward)
     int threads;
     int nv;          // 16-byte groups (or elements) per thread (row and ring kernels)
     int grid;        // persistent CTAs = rows of the partial buffer
     size_t smem_bytes;
     RingShape ring;
 };
-const void *bwd_ring_kernel_for(int dtype, int nv);
-BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, int sm_count);
+const void *bwd_ring_kernel_for(int dtype, int nv, bool dres);
+BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool dres, int sm_count);
 size_t bwd_partial_bytes(const BwdPlan &p, int H);
 cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, float *dweight,
                        cudaStream_t st);

@@ -132,3 +132,18 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(rn, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         rn.lib()
+
+
+def test_bwd_residual_invalid(lib):
+    D, R, XX, WW, RR, DX, DW = 0x100000, 0x180000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000
+
+    def bwd(**kw):
+        a = dict(dy=D, dr=R, x=XX, w=WW, rrms=RR, dx=DX, dw=DW, ws=0x700000, wsb=1 << 20, stride=64, M=4,
+                 H=64, dtype=2, has_w=1)
+        a.update(kw)
+        return lib.rmsnorm_bwd_residual(a["dy"], a["dr"], a["x"], a["w"], a["rrms"], a["dx"], a["dw"], a["ws"],
+                                        a["wsb"], a["stride"], a["M"], a["H"], a["dtype"], a["has_w"], None)
+
+    assert bwd(dr=None) == INVALID
+    assert bwd(dr=R + 1) == INVALID
+    assert bwd(M=0, dr=None, dw=None) == OK

@@ -199,6 +199,35 @@ def run_bwd(oracle, dtype, M, H, stride=None, weight=True, offset=0, eps=1e-5, s
     return out
 
 
+def run_bwd_residual(oracle, dtype, M, H, stride=None, weight=True, offset=0, eps=1e-5, seed=0):
+    """Fused forward, then the fused backward with an incoming residual-stream gradient."""
+    stride = H if stride is None else stride
+    rng = wl.rng_for(seed + 1000)
+    fwd = run_fwd(oracle, dtype, M, H, stride=stride, residual=True, weight=weight, offset=offset, eps=eps,
+                  seed=seed)
+    assert_fwd_ok(fwd)
+    s_np = fwd["gs"].host()
+    dy = wl.matrix(rng, M, H, dtype, stride)
+    dres = wl.matrix(rng, M, H, dtype, stride)
+    gdy = Guarded(M, H, stride, dtype, offset).upload(dy)
+    gdr = Guarded(M, H, stride, dtype, offset).upload(dres)
+    gdx = Guarded(M, H, stride, dtype, offset)
+    w = fwd["w"]
+    wd = device_vec(w, dtype, offset) if weight else None
+    dw = f32_buffer(H) if weight else None
+    nbytes = rn.rmsnorm_bwd_workspace_bytes(M, H, wl.torch_dtype(dtype))
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda") if dw is not None else None
+    rn.rmsnorm_bwd_residual(gdy.t, gdr.t, fwd["gs"].t, wd, fwd["rrms"], gdx.t, dw, ws)
+    torch.cuda.synchronize()
+    ref = oracle.rmsnorm_bwd(dy[:, :H], s_np, w, eps, dtype, dres=dres[:, :H])
+    got_dx = oracle.decode(gdx.host(), dtype) if dtype != "f32" else gdx.host().astype(np.float64)
+    out = {"dx": check_dx(got_dx, ref["dx"], ref["dx_scale"], bwd_rtol(dtype))}
+    if dw is not None:
+        out["dw"] = check_dweight(dw.cpu().numpy(), ref["dweight"], ref["dweight_abs"], bwd_rtol(dtype))
+    assert gdx.untouched_outside() and gdy.untouched_outside() and gdr.untouched_outside()
+    return out
+
+
 def assert_bwd_ok(out):
     assert out["dx"]["failed"] == 0, f"dx: {out['dx']['failed']} failed, max rel {out['dx']['max_rel']}"
     if "dw" in out:
@@ -287,3 +316,43 @@ def test_storage_widening_exhaustive(dtype, H, offset):
     nan_exp = 0x7C00 if dtype == "f16" else 0x7F80
     assert np.all(((got[isnan] & nan_exp) == nan_exp) & ((got[isnan] & (0x3FF if dtype == "f16" else 0x7F)) != 0))
     assert gs.untouched_outside() and gy.untouched_outside()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("H", [1, 64, 255, 1000, 2048, 4096, 4097, 6144, 8192, 16384])
+@pytest.mark.parametrize("weight", [True, False])
+def test_bwd_residual_paths(oracle, dtype, H, weight):
+    """Backward of the fused forward with the residual stream's gradient, every kernel path."""
+    assert_bwd_ok(run_bwd_residual(oracle, dtype, rows_for(H), H, weight=weight, seed=H + 3))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("H,stride,offset", [(4096, 4096, 1), (6144, 6272, 0), (1000, 1001, 1)])
+def test_bwd_residual_strides(oracle, dtype, H, stride, offset):
+    assert_bwd_ok(run_bwd_residual(oracle, dtype, rows_for(H, 200_000), H, stride=stride, offset=offset,
+                                   seed=stride))
+
+
+def test_bwd_residual_dweight_matches_plain_backward(oracle):
+    """The residual stream's gradient does not reach dweight: rmsnorm_bwd_residual's
+    dweight equals rmsnorm_bwd's up to summation order (the two entry points may run
+    different grids, hence different partial sums), i.e. within 1e-5 of sum |dy * xhat|."""
+    M, H = 513, 4096
+    rng = wl.rng_for(31)
+    x_np, w_np = wl.matrix(rng, M, H, "bf16"), wl.weight(rng, H, "bf16")
+    dy_np = wl.matrix(rng, M, H, "bf16")
+    x, w = wl.to_torch(x_np, "bf16").cuda(), wl.to_torch(w_np, "bf16").cuda()
+    dy = wl.to_torch(dy_np, "bf16").cuda()
+    dres = wl.to_torch(wl.matrix(rng, M, H, "bf16"), "bf16").cuda()
+    rrms = torch.empty(M, device="cuda")
+    rn.rmsnorm_fwd(x, w, torch.empty_like(x), rrms, eps=1e-5)
+    ws = torch.empty(rn.rmsnorm_bwd_workspace_bytes(M, H, torch.bfloat16), dtype=torch.uint8, device="cuda")
+    dw1, dw2 = torch.empty(H, device="cuda"), torch.empty(H, device="cuda")
+    dx1, dx2 = torch.empty_like(x), torch.empty_like(x)
+    rn.rmsnorm_bwd(dy, x, w, rrms, dx1, dw1, ws)
+    rn.rmsnorm_bwd_residual(dy, dres, x, w, rrms, dx2, dw2, ws)
+    torch.cuda.synchronize()
+    scale = oracle.rmsnorm_bwd(dy_np, x_np, w_np, 1e-5, "bf16", want_dx=False)["dweight_abs"]
+    diff = np.abs(dw1.cpu().numpy().astype(np.float64) - dw2.cpu().numpy())
+    assert np.all(diff <= 1e-5 * scale)
+    assert not torch.equal(dx1, dx2)
