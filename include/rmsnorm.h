@@ -37,7 +37,11 @@
  *     call returns a nonzero rmsn_status and launches nothing.  M == 0 is a
  *     valid no-op (row pointers and rrms may then be NULL).
  *   - An output may not overlap any other argument (byte ranges of the rows
- *     [0, M) are compared): in-place use is rejected with RMSN_ERR_ALIAS.
+ *     [0, M) are compared; RMSN_ERR_ALIAS), except in place: y may be x
+ *     itself, residual_out the residual itself, and dx may be dy, x or
+ *     dresidual_out itself (the same pointer; every element is read before
+ *     its thread writes it, and a row's reduction completes before any of
+ *     the row is written).  Partial overlaps are always rejected.
  */
 #ifndef RMSNORM_GB300_H
 #define RMSNORM_GB300_H

@@ -136,9 +136,14 @@ int forward(const void *x, const void *residual, const void *weight, void *y, vo
     const Range rq = bytes_of(rrms, (size_t)M * sizeof(float));
     const Range outs[] = {ry, rs, rq};
     const Range all[] = {rx, rr, rw, ry, rs, rq};
+    // in place: y may be x itself and residual_out the residual itself
+    // (every element is read before its thread writes it)
+    const bool same[3][6] = {{y == x, false, false, false, false, false},
+                             {false, fused && residual_out == residual, false, false, false, false},
+                             {false, false, false, false, false, false}};
     for (int o = 0; o < 3; ++o)
         for (int k = 0; k < 6; ++k)
-            if (k != 3 + o && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
+            if (k != 3 + o && !same[o][k] && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
 
     if (M == 0) return RMSN_OK;
     int dev = 0, sms = 0;
@@ -307,9 +312,13 @@ int backward(const void *dy, const void *dres, const void *x, const void *weight
     const Range rws = bytes_of(dw != nullptr ? workspace : nullptr, part_bytes);
     const Range outs[] = {rdx, rdw, rws};
     const Range all[] = {rdy, rx, rw, rq, rdr, rdx, rdw, rws};
+    // in place: dx may be dy, x or dresidual_out itself (each element of a
+    // row is read before its thread writes dx there; the row's reduction
+    // completes before any dx of the row is written)
+    const bool same_dx[8] = {dx == dy, dx == x, false, false, dr != nullptr && dx == dr, false, false, false};
     for (int o = 0; o < 3; ++o)
         for (int k = 0; k < 8; ++k)
-            if (k != 5 + o && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
+            if (k != 5 + o && !(o == 0 && same_dx[k]) && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
 
     BwdArgs a{};
     a.err = device_error_word(dev);

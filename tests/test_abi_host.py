@@ -77,13 +77,21 @@ def test_fwd_residual_invalid(lib, kw):
 
 
 @pytest.mark.parametrize("kw", [
-    dict(y=X), dict(y=X + 2 * 64 * 3), dict(rrms=X + 8), dict(y=W), dict(rrms=Y + 100),
+    dict(y=X + 2), dict(y=X + 2 * 64 * 3), dict(rrms=X + 8), dict(y=W), dict(rrms=Y + 100),
 ])
 def test_fwd_alias(lib, kw):
     assert fwd(lib, **kw) == ALIAS
 
 
-@pytest.mark.parametrize("kw", [dict(s=R), dict(s=Y), dict(y=R + 64), dict(rrms=S)])
+def test_exact_in_place_is_accepted(lib):
+    # same pointer: validated, then (M = 0) nothing launched
+    assert fwd(lib, y=X, M=0) == OK
+    assert fwd_res(lib, y=X, s=R, M=0) == OK
+    assert fwd_res(lib, s=R + 2, M=4) == ALIAS        # partial overlap stays rejected
+    assert fwd_res(lib, y=R, M=4) == ALIAS            # y over the residual is not in place
+
+
+@pytest.mark.parametrize("kw", [dict(s=X), dict(s=Y), dict(y=R + 64), dict(rrms=S)])
 def test_fwd_residual_alias(lib, kw):
     assert fwd_res(lib, **kw) == ALIAS
 

@@ -288,11 +288,52 @@ def test_workspace_too_small():
     assert e.value.status == 3
 
 
-def test_in_place_rejected():
+def test_partial_overlap_rejected():
     x = torch.randn(64, 1024, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(rn.RmsnormError) as e:
-        rn.rmsnorm_fwd(x, None, x)
+        rn.rmsnorm_fwd(x[:, :1000], None, x[:, 8:1008])
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("H,offset", [(64, 0), (255, 0), (1000, 0), (2048, 0), (4096, 0), (4097, 0), (8192, 0),
+                                      (32768, 0), (4096, 1)])
+def test_in_place_matches_out_of_place(dtype, H, offset):
+    """y over x and residual_out over the residual (forward), dx over dy or over
+    dresidual_out (backward): the same bits as with separate outputs, guard
+    bands intact, on every kernel path."""
+    M = rows_for(H, 200_000)
+    rng = wl.rng_for(H + offset)
+    xs, rs = wl.matrix(rng, M, H, dtype), wl.matrix(rng, M, H, dtype)
+    w = device_vec(wl.weight(rng, H, dtype), dtype, offset)
+    dys, drs = wl.matrix(rng, M, H, dtype), wl.matrix(rng, M, H, dtype)
+    G = lambda a=None: Guarded(M, H, H, dtype, offset) if a is None else Guarded(M, H, H, dtype, offset).upload(a)
+    # out of place
+    x, r, y, so = G(xs), G(rs), G(), G()
+    rr = f32_buffer(M, offset)
+    rn.rmsnorm_fwd_residual(x.t, r.t, w, y.t, so.t, rr, eps=1e-5)
+    # in place
+    xi, ri = G(xs), G(rs)
+    rri = f32_buffer(M, offset)
+    rn.rmsnorm_fwd_residual(xi.t, ri.t, w, xi.t, ri.t, rri, eps=1e-5)
+    torch.cuda.synchronize()
+    assert torch.equal(xi.t, y.t) and torch.equal(ri.t, so.t) and torch.equal(rri, rr)
+    assert xi.untouched_outside() and ri.untouched_outside()
+
+    nbytes = rn.rmsnorm_bwd_workspace_bytes(M, H, wl.torch_dtype(dtype))
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+    dy, dx, dw = G(dys), G(), f32_buffer(H)
+    rn.rmsnorm_bwd(dy.t, so.t, w, rr, dx.t, dw, ws)
+    dyi, dwi = G(dys), f32_buffer(H)
+    rn.rmsnorm_bwd(dyi.t, so.t, w, rr, dyi.t, dwi, ws)            # dx over dy
+    dr, dx2, dw2 = G(drs), G(), f32_buffer(H)
+    rn.rmsnorm_bwd_residual(dy.t, dr.t, so.t, w, rr, dx2.t, dw2, ws)
+    dri, dw2i = G(drs), f32_buffer(H)
+    rn.rmsnorm_bwd_residual(dy.t, dri.t, so.t, w, rr, dri.t, dw2i, ws)   # dx over dresidual_out
+    torch.cuda.synchronize()
+    assert torch.equal(dyi.t, dx.t) and torch.equal(dwi, dw)
+    assert torch.equal(dri.t, dx2.t) and torch.equal(dw2i, dw2)
+    assert dyi.untouched_outside() and dri.untouched_outside()
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
