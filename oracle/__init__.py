@@ -67,8 +67,9 @@ def _load():
             lib.orc_rmsnorm_fwd.argtypes = [i32, p, p, p, i64, i64, i64, d, p, p, p, i32]
             lib.orc_rmsnorm_bwd.argtypes = [i32, p, p, p, i64, i64, i64, d, p, p, p, p, p, i32]
             lib.orc_rmsnorm_bwd_residual.argtypes = [i32, p, p, p, p, i64, i64, i64, d, p, p, p, p, p, i32]
+            lib.orc_rmsnorm_adaln_fwd.argtypes = [i32, p, p, p, p, i64, i64, i64, i64, i64, d, p, p, p, i32]
             for f in (lib.orc_decode, lib.orc_encode, lib.orc_rmsnorm_fwd, lib.orc_rmsnorm_bwd,
-                      lib.orc_rmsnorm_bwd_residual):
+                      lib.orc_rmsnorm_bwd_residual, lib.orc_rmsnorm_adaln_fwd):
                 f.restype = i32
             _lib = lib
     return _lib
@@ -207,3 +208,33 @@ def rmsnorm_bwd(dy, x, w, eps: float, dtype: str, want_dx: bool = True,
     if rc:
         raise ValueError(f"orc_rmsnorm_bwd failed ({rc})")
     return {"dx": dx, "dx_scale": dx_scale, "dweight": dweight, "dweight_abs": dweight_abs, "rrms": rrms}
+
+
+def rmsnorm_adaln_fwd(x, w, scale, shift, eps: float, dtype: str, rows_per_cond: int = 1,
+                      nthreads: int | None = None):
+    """AdaLN forward: norm(x) * w * (1 + scale) + shift ("Rocm Kernels" page,
+    4. AdaLN).  x: (M, H) storage; scale, shift: (ceil(M / rows_per_cond), H)
+    storage conditioning rows (token row i uses row i // rows_per_cond);
+    w: (H,) or None.  Returns float64 ``y`` (M, H), ``y_scale`` (M, H: size of
+    the two terms whose sum is y) and ``rrms`` (M,)."""
+    x, M, H, stride = _matrix(x, dtype, "x")
+    scale, Ms, Hs, cs = _matrix(scale, dtype, "scale")
+    shift, Mh, Hh, ch = _matrix(shift, dtype, "shift")
+    need = (M + rows_per_cond - 1) // rows_per_cond
+    if Hs != H or Hh != H or Ms < need or Mh < need:
+        raise ValueError("scale/shift must hold ceil(M / rows_per_cond) rows of H")
+    if cs != ch:
+        scale, shift = np.ascontiguousarray(scale), np.ascontiguousarray(shift)
+        cs = H
+    if w is not None:
+        w = np.ascontiguousarray(w)
+        _check_storage(w, dtype, "w")
+    y = np.empty((M, H), np.float64)
+    y_scale = np.empty((M, H), np.float64)
+    rrms = np.empty((M,), np.float64)
+    rc = _load().orc_rmsnorm_adaln_fwd(DTYPES[dtype], _ptr(x), _ptr(w), _ptr(scale), _ptr(shift), M, H, stride,
+                                       cs, rows_per_cond, eps_as_f32(eps), _ptr(y), _ptr(y_scale), _ptr(rrms),
+                                       nthreads or default_threads())
+    if rc:
+        raise ValueError(f"orc_rmsnorm_adaln_fwd failed ({rc})")
+    return {"y": y, "y_scale": y_scale, "rrms": rrms}

@@ -293,6 +293,68 @@ int orc_rmsnorm_fwd(int dtype, const void *x, const void *r, const void *w,
 }
 
 /* ------------------------------------------------------------------------ */
+/* AdaLN forward ("Rocm Kernels" page, section 4. AdaLN / Template 4):      */
+/*   out = norm(x) * weight * (1 + scale) + shift                           */
+/* evaluated left to right on norm(x) = x * rrms; scale and shift are       */
+/* conditioning rows: token row i uses conditioning row i / rows_per_cond   */
+/* (1 = per token, [B, S, H]; S = one row per sequence, [B, 1, H]).         */
+/* ------------------------------------------------------------------------ */
+
+struct adaln_ctx {
+    int dtype;
+    const void *x, *w, *scale, *shift;
+    int64_t H, stride, cond_stride, rows_per_cond;
+    double eps;
+    double *y, *y_scale, *rrms;
+};
+
+static void adaln_rows(void *p, int64_t i0, int64_t i1)
+{
+    const struct adaln_ctx *c = (const struct adaln_ctx *)p;
+    const int64_t H = c->H;
+    for (int64_t i = i0; i < i1; ++i) {
+        const int64_t row = i * c->stride;
+        const int64_t crow = (i / c->rows_per_cond) * c->cond_stride;
+        double ss = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            const double v = load_elem(c->dtype, c->x, row + h);
+            ss += v * v;
+        }
+        const double rrms = 1.0 / sqrt(ss / (double)H + c->eps);
+        if (c->rrms)
+            c->rrms[i] = rrms;
+        for (int64_t h = 0; h < H; ++h) {
+            const double w = c->w ? load_elem(c->dtype, c->w, h) : 1.0;
+            const double sc = load_elem(c->dtype, c->scale, crow + h);
+            const double sh = load_elem(c->dtype, c->shift, crow + h);
+            const double t = ((load_elem(c->dtype, c->x, row + h) * rrms) * w) * (1.0 + sc);
+            c->y[i * H + h] = t + sh;
+            /* size of the two terms whose sum is y (bounds any rounding order) */
+            if (c->y_scale)
+                c->y_scale[i * H + h] = fabs(t) + fabs(sh);
+        }
+    }
+}
+
+/*
+ * x: M x H at `stride`; scale, shift: conditioning rows at `cond_stride`;
+ * w nullable (no weight).  Outputs y (dense M x H), y_scale (nullable),
+ * rrms (nullable).
+ */
+int orc_rmsnorm_adaln_fwd(int dtype, const void *x, const void *w, const void *scale, const void *shift,
+                          int64_t M, int64_t H, int64_t stride, int64_t cond_stride, int64_t rows_per_cond,
+                          double eps, double *y, double *y_scale, double *rrms, int nthreads)
+{
+    if (!elem_size(dtype) || !x || !scale || !shift || !y || M < 0 || H <= 0 || stride < H ||
+        cond_stride < H || rows_per_cond < 1)
+        return 1;
+    struct adaln_ctx c = {dtype, x, w, scale, shift, H, stride, cond_stride, rows_per_cond, eps, y, y_scale,
+                          rrms};
+    parallel_ranges(adaln_rows, &c, M, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Backward                                                                 */
 /* ------------------------------------------------------------------------ */
 

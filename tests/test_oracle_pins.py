@@ -308,3 +308,51 @@ def test_fused_backward_central_differences(oracle, M, H):
     plain = oracle.rmsnorm_bwd(dy, x + r, w, eps, "f64")
     np.testing.assert_allclose(out["dweight"], plain["dweight"], rtol=0, atol=0)   # dres does not reach w
     assert np.all(out["dx_scale"] >= np.abs(out["dx"]))
+
+
+# ------------------------------------------------------------------ AdaLN --
+
+def test_adaln_reduces_to_rmsnorm(oracle):
+    """scale = shift = 0: AdaLN is the plain forward, bit for bit."""
+    rng = np.random.default_rng(40)
+    x = rng.standard_normal((6, 48))
+    w = 1 + 0.1 * rng.standard_normal(48)
+    z = np.zeros((6, 48))
+    a = oracle.rmsnorm_adaln_fwd(x, w, z, z, 1e-5, "f64")
+    b = oracle.rmsnorm_fwd(x, w, 1e-5, "f64")
+    assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["rrms"], b["rrms"])
+
+
+def test_adaln_scale_and_shift_are_affine(oracle):
+    """out = (1 + scale) * norm(x) * w + shift, per column and per conditioning row."""
+    rng = np.random.default_rng(41)
+    M, H = 5, 40
+    x = rng.standard_normal((M, H))
+    w = 1 + 0.1 * rng.standard_normal(H)
+    sc = rng.standard_normal((M, H))
+    sh = rng.standard_normal((M, H))
+    plain = oracle.rmsnorm_fwd(x, w, 1e-5, "f64")["y"]
+    got = oracle.rmsnorm_adaln_fwd(x, w, sc, sh, 1e-5, "f64")["y"]
+    np.testing.assert_allclose(got, plain * (1 + sc) + sh, rtol=1e-13, atol=1e-13)
+
+
+def test_adaln_broadcast_conditioning_rows(oracle):
+    """rows_per_cond = S: the [B, 1, H] form equals the [B, S, H] form with the rows repeated."""
+    rng = np.random.default_rng(42)
+    B, S, H = 3, 4, 24
+    x = rng.standard_normal((B * S, H))
+    sc, sh = rng.standard_normal((B, H)), rng.standard_normal((B, H))
+    a = oracle.rmsnorm_adaln_fwd(x, None, sc, sh, 1e-6, "f64", rows_per_cond=S)["y"]
+    b = oracle.rmsnorm_adaln_fwd(x, None, np.repeat(sc, S, axis=0), np.repeat(sh, S, axis=0), 1e-6, "f64")["y"]
+    assert np.array_equal(a, b)
+
+
+def test_adaln_closed_form_single_column(oracle):
+    """H = 1: out = x w (1 + s) / sqrt(x^2 + eps) + shift."""
+    x = np.array([[2.0], [-0.5]])
+    sc, sh = np.array([[0.25], [-1.5]]), np.array([[1.0], [3.0]])
+    e = oracle.eps_as_f32(1e-3)
+    got = oracle.rmsnorm_adaln_fwd(x, np.array([0.8]), sc, sh, 1e-3, "f64")
+    want = x[:, 0] * 0.8 * (1 + sc[:, 0]) / np.sqrt(x[:, 0] ** 2 + e) + sh[:, 0]
+    np.testing.assert_allclose(got["y"][:, 0], want, rtol=1e-15)
+    assert np.all(got["y_scale"] >= np.abs(got["y"]))
