@@ -391,6 +391,82 @@ class DitMixWorkload:
         return rows * self.call_bytes_w / self.M
 
 
+class AdalnWorkload:
+    """AdaLN forward of a DiT block: y = norm(x) * w * (1 + scale) + shift on
+    2 sequences x 6144 tokens x 2048 bf16 (the video-DiT token shape of the
+    168-call mix), one conditioning row per sequence broadcast over its
+    tokens.  Eight calls per step over four rotating x/y buffer sets, so that
+    no call finds its operands in L2."""
+    name = "adaln_bf16_2x6144x2048_per_sequence"
+    flush_l2 = False
+    n_calls, n_sets = 8, 4
+
+    def __init__(self):
+        import torch
+        import residual_add_rmsnorm_fwd_gb300 as rn
+        import workloads as wl
+        self.torch, self.rn, self.wl = torch, rn, wl
+        self.B, self.T, self.H, self.dt, self.eps = 2, 6144, 2048, "bf16", 1e-6
+        self.M, self.S = self.B * self.T, self.H
+        self.es = wl.ELEM_BYTES[self.dt]
+        rng = wl.rng_for(40)
+        self.host = {"xs": [wl.matrix(rng, self.M, self.H, self.dt) for _ in range(self.n_sets)],
+                     "w": wl.weight(rng, self.H, self.dt),
+                     "scale": wl.conditioning(rng, self.B, self.H, self.dt),
+                     "shift": wl.conditioning(rng, self.B, self.H, self.dt)}
+        self.call_bytes = 2 * self.M * self.H * self.es + 3 * self.B * self.H * self.es + self.H * self.es
+        self.bytes_per_step = self.n_calls * self.call_bytes
+        self.rows_per_step = self.n_calls * self.M
+        self.kernels_per_step = self.n_calls
+
+    def _make_set(self):
+        from types import SimpleNamespace
+        torch, wl, dt = self.torch, self.wl, self.dt
+        dev = torch.device("cuda")
+        b = SimpleNamespace()
+        b.xs = [wl.to_torch(a, dt).to(dev) for a in self.host["xs"]]
+        b.ys = [torch.empty_like(x) for x in b.xs]
+        return b
+
+    def setup(self):
+        dev = self.torch.device("cuda")
+        up = lambda a: self.wl.to_torch(a, self.dt).to(dev)  # noqa: E731
+        self.w, self.sc, self.sh = up(self.host["w"]), up(self.host["scale"]), up(self.host["shift"])
+        self.sets = [self._make_set()]
+        return self
+
+    def calls(self, k=0):
+        rn, b = self.rn, self.sets[k]
+        return [("adaln", lambda x=b.xs[i % self.n_sets], y=b.ys[i % self.n_sets]: rn.rmsnorm_adaln_fwd(
+                    x, self.w, self.sc, self.sh, y, rows_per_cond=self.T, eps=self.eps), self.call_bytes)
+                for i in range(self.n_calls)]
+
+    def config(self):
+        return {"workload": self.name, "M": self.M, "H": self.H, "B": self.B, "T": self.T, "dtype": self.dt,
+                "rows_per_cond": self.T, "calls_per_step": self.n_calls, "eps": self.eps,
+                "l2": f"{self.n_sets} rotating x/y buffer sets of {2 * self.M * self.H * self.es} bytes",
+                "algorithmic_bytes_per_step": self.bytes_per_step}
+
+    def e2e_setup(self):
+        torch, b = self.torch, self.sets[0]
+        self.h_in = [x.cpu().pin_memory() for x in b.xs]
+        self.h_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in b.ys]
+        while len(self.sets) < 2:
+            self.sets.append(self._make_set())
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h_in)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
+
+    def e2e_transfers(self, k):
+        b = self.sets[k]
+        return list(zip(b.xs, self.h_in)), list(zip(self.h_out, b.ys))
+
+    def oracle_step(self, rows):
+        import oracle
+        oracle.rmsnorm_adaln_fwd(self.host["xs"][0][:rows], self.host["w"], self.host["scale"][:1],
+                                 self.host["shift"][:1], self.eps, self.dt, rows_per_cond=self.T)
+        return rows * self.call_bytes / self.M
+
+
 class SmallFwdWorkload(StepWorkload):
     """The fp32 forward on 64 x 1024 rows: 528 KB, resident in L2 unless
     flushed, so L2 is flushed before every step and only the kernel's own
@@ -405,6 +481,7 @@ class SmallFwdWorkload(StepWorkload):
 WORKLOADS = {
     "fwd_f32_small": SmallFwdWorkload,
     "dit_mix": DitMixWorkload,
+    "adaln": AdalnWorkload,
     "step": lambda: StepWorkload(2, backward=True),
     "fused_fwd": lambda: StepWorkload(2, backward=False),
     "fused_fwd_bwd_residual": lambda: StepWorkload(2, backward=True, dres=True),

@@ -106,6 +106,33 @@ int rmsnorm_fwd_residual(const void *x, const void *residual, const void *weight
                          int dtype, int has_weight, void *stream);
 
 /*
+ * AdaLN forward: the norm followed by the DiT block's adaptive conditioning,
+ * in one pass ("Rocm Kernels" page, 4. AdaLN, and its Kernel-Specific
+ * Guidelines, AdaLN):
+ *   y = (x * rrms) * weight * (1 + scale) + shift
+ * with rrms as in rmsnorm_fwd, every step in binary32 and one rounding of y
+ * to the storage type.  Row i reads conditioning row c = i / rows_per_cond
+ * (integer division) of scale and shift:
+ *   - rows_per_cond == 1: per-token conditioning, scale and shift of shape
+ *     [batch, seq, H] flattened to M rows;
+ *   - rows_per_cond == seq: one conditioning row per sequence, scale and
+ *     shift of shape [batch, 1, H] broadcast over the sequence's rows (the
+ *     second shape the page accepts; rows of one sequence are consecutive).
+ *   x             in   M x H, row_stride
+ *   weight        in   H elements; ignored when has_weight == 0
+ *   scale, shift  in   ceil(M / rows_per_cond) x H, cond_stride >= H
+ *   y             out  M x H, row_stride (may be x itself)
+ *   rrms          out  M binary32 values (NULL = not saved)
+ *   rows_per_cond >= 1.  128-bit accesses additionally need cond_stride
+ *   times the element size a multiple of 16 and 16-byte aligned scale and
+ *   shift.  No backward is provided for this call.
+ */
+int rmsnorm_adaln_fwd(const void *x, const void *weight, const void *scale, const void *shift,
+                      void *y, float *rrms, int64_t row_stride, int64_t cond_stride,
+                      int64_t rows_per_cond, int64_t M, int64_t H, float eps,
+                      int dtype, int has_weight, void *stream);
+
+/*
  * Size in bytes of the workspace rmsnorm_bwd (and rmsnorm_bwd_residual)
  * needs for (M, H, dtype) on the current device (per-CTA binary32 dweight
  * partials).  Writes *bytes; the

@@ -22,7 +22,7 @@ import threading
 
 __all__ = [
     "RMSN_F32", "RMSN_F16", "RMSN_BF16", "RmsnormError", "lib", "lib_path",
-    "rmsnorm_fwd", "rmsnorm_fwd_residual", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
+    "rmsnorm_fwd", "rmsnorm_fwd_residual", "rmsnorm_adaln_fwd", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
     "rmsnorm_bwd_residual", "rmsnorm_bwd_noalloc", "rmsnorm_read_device_errors", "rmsnorm_status_string",
     "dtype_code",
 ]
@@ -61,6 +61,7 @@ def lib():
                                    ctypes.c_size_t)
             L.rmsnorm_fwd.argtypes = [p, p, p, p, i64, i64, i64, f32, i32, i32, p]
             L.rmsnorm_fwd_residual.argtypes = [p, p, p, p, p, p, i64, i64, i64, f32, i32, i32, p]
+            L.rmsnorm_adaln_fwd.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64, f32, i32, i32, p]
             L.rmsnorm_bwd_workspace_bytes.argtypes = [i64, i64, i32, ctypes.POINTER(sz)]
             L.rmsnorm_bwd.argtypes = [p, p, p, p, p, p, p, sz, i64, i64, i64, i32, i32, p]
             L.rmsnorm_bwd_residual.argtypes = [p, p, p, p, p, p, p, p, sz, i64, i64, i64, i32, i32, p]
@@ -140,6 +141,23 @@ def rmsnorm_fwd_residual(x, residual, weight, y, residual_out, rrms=None, eps: f
     _check("rmsnorm_fwd_residual", lib().rmsnorm_fwd_residual(
         _ptr(x), _ptr(residual), _ptr(weight), _ptr(y), _ptr(residual_out), _ptr(rrms), stride, M, H,
         float(eps), dtype_code(x.dtype), int(weight is not None), _stream(stream)))
+
+
+def rmsnorm_adaln_fwd(x, weight, scale, shift, y, rows_per_cond: int = 1, rrms=None, eps: float = 1e-6,
+                      stream=None):
+    """y = norm(x) * weight * (1 + scale) + shift.  ``scale`` and ``shift``
+    are (ceil(M / rows_per_cond), H) with one shared row stride: row i of x
+    uses their row i // rows_per_cond (1 = per-token conditioning, seq = one
+    row per sequence broadcast over it)."""
+    M, H, stride = _shared_stride([(x, "x"), (y, "y")])
+    n_cond, h, cond_stride = _shared_stride([(scale, "scale"), (shift, "shift")])
+    if h != H:
+        raise ValueError(f"scale/shift: {h} columns, x has {H}")
+    if rows_per_cond < 1 or n_cond != -(-M // rows_per_cond):
+        raise ValueError(f"scale/shift: {n_cond} rows for M={M}, rows_per_cond={rows_per_cond}")
+    _check("rmsnorm_adaln_fwd", lib().rmsnorm_adaln_fwd(
+        _ptr(x), _ptr(weight), _ptr(scale), _ptr(shift), _ptr(y), _ptr(rrms), stride, cond_stride,
+        int(rows_per_cond), M, H, float(eps), dtype_code(x.dtype), int(weight is not None), _stream(stream)))
 
 
 def rmsnorm_read_device_errors() -> int:

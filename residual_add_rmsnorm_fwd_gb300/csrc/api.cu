@@ -111,6 +111,18 @@ bool rows_vectorisable(int64_t H, int64_t stride, int dtype) {
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA; }
 
+// Kernel family by row length and layout: lane groups below 256 elements
+// (plain and residual-fused; AdaLN takes the register kernel there), the
+// bulk-copy ring for aligned rows of at least 8 KB, the register kernel, and
+// the two-pass chunked kernel above the register budget.
+int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, int sms, cudaStream_t s) {
+    if (a.H < kSmallH && mode != kAdaln) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
+    RingPlan ring;
+    if (vec && plan_fwd_ring(a.M, a.H, dtype, mode, sms, &ring)) return to_status(launch_fwd_ring(a, dtype, mode, ring, s));
+    if (fwd_row_fits(a.H, dtype, vec)) return to_status(launch_fwd_row(a, dtype, mode, vec, sms, s));
+    return to_status(launch_fwd_chunked(a, dtype, mode, vec, sms, s));
+}
+
 int forward(const void *x, const void *residual, const void *weight, void *y, void *residual_out,
             float *rrms, int64_t row_stride, int64_t M, int64_t H, float eps, int dtype, int has_weight,
             void *stream, bool fused) {
@@ -167,13 +179,67 @@ int forward(const void *x, const void *residual, const void *weight, void *y, vo
     a.H = (int)H;
     a.eps = eps;
     a.has_w = has_weight ? 1 : 0;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (H < kSmallH) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
-    RingPlan ring;
-    if (vec && plan_fwd_ring(M, (int)H, dtype, fused, sms, &ring))
-        return to_status(launch_fwd_ring(a, dtype, ring, s));
-    if (fwd_row_fits((int)H, dtype, vec)) return to_status(launch_fwd_row(a, dtype, vec, sms, s));
-    return to_status(launch_fwd_chunked(a, dtype, vec, sms, s));
+    return dispatch_fwd(a, dtype, fused ? kResid : kPlain, vec, sms, static_cast<cudaStream_t>(stream));
+}
+
+// AdaLN forward: rows use conditioning row i / rows_per_cond of scale and
+// shift (n_cond = ceil(M / rows_per_cond) rows of cond_stride elements).
+int adaln_forward(const void *x, const void *weight, const void *scale, const void *shift, void *y, float *rrms,
+                  int64_t row_stride, int64_t cond_stride, int64_t rows_per_cond, int64_t M, int64_t H, float eps,
+                  int dtype, int has_weight, void *stream) {
+    int st = check_shape(M, H, row_stride, dtype);
+    if (st) return st;
+    if (!std::isfinite(eps) || eps < 0.0f) return RMSN_ERR_INVALID;
+    if (has_weight && weight == nullptr) return RMSN_ERR_INVALID;
+    if (rows_per_cond < 1 || cond_stride < H) return RMSN_ERR_INVALID;
+    const int64_t n_cond = M > 0 ? (M - 1) / rows_per_cond + 1 : 0;
+    if ((st = check_shape(n_cond, H, cond_stride, dtype))) return st;
+    if (M > 0 && (x == nullptr || y == nullptr || scale == nullptr || shift == nullptr)) return RMSN_ERR_INVALID;
+    const int es = elem_bytes(dtype);
+    const void *w = has_weight ? weight : nullptr;
+    for (const void *p : {x, w, scale, shift, static_cast<const void *>(y)})
+        if (p != nullptr && !aligned(p, es)) return RMSN_ERR_INVALID;
+    if (rrms != nullptr && !aligned(rrms, 4)) return RMSN_ERR_INVALID;
+
+    const Range rx = matrix_of(x, M, H, row_stride, es);
+    const Range rw = bytes_of(w, (size_t)H * es);
+    const Range rsc = matrix_of(scale, n_cond, H, cond_stride, es);
+    const Range rsh = matrix_of(shift, n_cond, H, cond_stride, es);
+    const Range ry = matrix_of(y, M, H, row_stride, es);
+    const Range rq = bytes_of(rrms, (size_t)M * sizeof(float));
+    const Range outs[] = {ry, rq};
+    const Range all[] = {rx, rw, rsc, rsh, ry, rq};
+    // in place: y may be x itself (scale and shift may be shared by rows,
+    // so they are never overwritten)
+    for (int o = 0; o < 2; ++o)
+        for (int k = 0; k < 6; ++k)
+            if (k != 4 + o && !(o == 0 && k == 0 && y == x) && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
+
+    if (M == 0) return RMSN_OK;
+    int dev = 0, sms = 0;
+    st = current_device(&dev, &sms);
+    if (st) return st;
+
+    bool vec = rows_vectorisable(H, row_stride, dtype) && (cond_stride * es) % 16 == 0;
+    for (const void *p : {x, w, scale, shift, static_cast<const void *>(y)})
+        if (p != nullptr && !aligned(p, 16)) vec = false;
+
+    FwdArgs a{};
+    a.err = device_error_word(dev);
+    a.x = x;
+    a.w = w;
+    a.y = y;
+    a.rrms = rrms;
+    a.stride = row_stride;
+    a.M = M;
+    a.H = (int)H;
+    a.eps = eps;
+    a.has_w = has_weight ? 1 : 0;
+    a.scale = scale;
+    a.shift = shift;
+    a.cond_stride = cond_stride;
+    a.rows_per_cond = rows_per_cond;
+    return dispatch_fwd(a, dtype, kAdaln, vec, sms, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -216,14 +282,17 @@ void finish_ring(RingPlan *p, int nv, int threads, int64_t row_bytes, int stream
 // 1024 groups), two stages, two CTAs per SM: measured best at H = 4096-8192
 // (deeper rings or more CTAs per SM put more rows in flight and lose DRAM
 // efficiency); shorter rows run faster on the register kernel.
-bool fwd_ring_geometry(int H, int dtype, bool resid, RingPlan *p) {
+bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
     const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
     if (row_bytes % 16 != 0 || row_bytes < 8192) return false;
     const int nvec = (int)(row_bytes / 16);
     const int nv = nvec <= 1024 ? 2 : 4;
     const int threads = round_up_to(ceil_div(nvec, nv), 32);
     if (threads > 512) return false;
-    finish_ring(p, nv, threads, row_bytes, resid ? 2 : 1, 2, 2);
+    const int streams = mode == kAdaln ? 3 : (mode == kResid ? 2 : 1);   // x (+ residual | scale, shift)
+    const int stages = 2;
+    if (kRingHeaderBytes + (size_t)stages * streams * round_up_to((int)row_bytes, 128) > 200 * 1024) return false;
+    finish_ring(p, nv, threads, row_bytes, streams, stages, 2);
     return true;
 }
 
@@ -357,6 +426,13 @@ RMSN_API int rmsnorm_fwd_residual(const void *x, const void *residual, const voi
                          int has_weight, void *stream) {
     return forward(x, residual, weight, y, residual_out, rrms, row_stride, M, H, eps, dtype, has_weight, stream,
                    true);
+}
+
+RMSN_API int rmsnorm_adaln_fwd(const void *x, const void *weight, const void *scale, const void *shift, void *y,
+                               float *rrms, int64_t row_stride, int64_t cond_stride, int64_t rows_per_cond,
+                               int64_t M, int64_t H, float eps, int dtype, int has_weight, void *stream) {
+    return adaln_forward(x, weight, scale, shift, y, rrms, row_stride, cond_stride, rows_per_cond, M, H, eps, dtype,
+                         has_weight, stream);
 }
 
 RMSN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype, size_t *bytes) {

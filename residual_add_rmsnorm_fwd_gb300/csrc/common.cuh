@@ -28,7 +28,15 @@ struct FwdArgs {
     float eps;
     int has_w;
     unsigned *err;        // device error word (bounded pipeline waits report here)
+    // AdaLN conditioning: token row i reads scale/shift row i / rows_per_cond
+    const void *scale;
+    const void *shift;
+    int64_t cond_stride;
+    int64_t rows_per_cond;
 };
+
+// Forward variants: plain norm, residual-fused, AdaLN (norm * w * (1 + scale) + shift).
+enum FwdMode { kPlain = 0, kResid = 1, kAdaln = 2 };
 
 struct BwdArgs {
     const void *dy;

@@ -1,24 +1,29 @@
-// fwd_chunked.cu -- RMSNorm forward (plain and residual-fused) for hidden
-// sizes above the register budget of the row kernel.
+// fwd_chunked.cu -- RMSNorm forward (plain, residual-fused, AdaLN) for
+// hidden sizes above the register budget of the row kernel.
 //
 // Two passes over each row with identical chunk bounds ("Skill: Write a
 // Triton RMSNorm Kernel", Required reasoning 11; Kernel design rules, last
 // rule): pass 1 accumulates the binary32 sum of squares chunk by chunk;
 // pass 2 re-reads the chunks (the row was just read, so the re-read is
 // mostly served by L2), recomputes the identical binary32 s = x + residual,
-// and writes residual_out and y.  One CTA per row, persistent grid.
+// and writes residual_out and y (AdaLN: y * (1 + scale) + shift, "Rocm
+// Kernels" page, 4. AdaLN).  One CTA per row, persistent grid.
 #include "launch.h"
 
 namespace rmsn {
 
-template <typename T, int VEC, bool RESID>
+template <typename T, int VEC, int MODE>
 __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
+    constexpr bool RESID = MODE == kResid;
+    constexpr bool ADALN = MODE == kAdaln;
     using P = Pack<T, VEC>;
     constexpr int U = 2;  // vectors per thread per chunk (independent loads in flight)
     __shared__ float red[64];
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
+    const T *__restrict__ scale = static_cast<const T *>(a.scale);
+    const T *__restrict__ shift = static_cast<const T *>(a.shift);
     T *__restrict__ y = static_cast<T *>(a.y);
     T *__restrict__ s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
@@ -28,6 +33,7 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
     int bank = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * a.stride;
+        const int64_t cbase = ADALN ? (row / a.rows_per_cond) * a.cond_stride : 0;
         float ss = 0.0f;
         for (int c0 = 0; c0 < nvec; c0 += chunk) {
             P xp[U], rp[U];
@@ -62,7 +68,7 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
         if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[row] = rrms;
 
         for (int c0 = 0; c0 < nvec; c0 += chunk) {
-            P xp[U], rp[U], wp[U];
+            P xp[U], rp[U], wp[U], scp[U], shp[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * blockDim.x + threadIdx.x;
@@ -70,6 +76,10 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
                     xp[u] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
                     if constexpr (RESID) rp[u] = ld_stream<T, VEC>(r + base + (int64_t)c * VEC);
                     wp[u] = a.has_w ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+                    if constexpr (ADALN) {
+                        scp[u] = ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC);
+                        shp[u] = ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC);
+                    }
                 }
             }
 #pragma unroll
@@ -88,6 +98,13 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
                     unpack(wp[u], wv);
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
+                    if constexpr (ADALN) {   // y * (1 + scale) + shift
+                        float sc[VEC], sh[VEC];
+                        unpack(scp[u], sc);
+                        unpack(shp[u], sh);
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) v[j] = fmaf(v[j], 1.0f + sc[j], sh[j]);
+                    }
                     st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
                 }
             }
@@ -99,30 +116,38 @@ namespace {
 
 constexpr int kThreads = 512;
 
-template <typename T, int VEC, bool RESID>
+template <typename T, int VEC, int MODE>
 cudaError_t launch_t(const FwdArgs &a, int sm_count, cudaStream_t st) {
-    auto k = fwd_chunked_kernel<T, VEC, RESID>;
+    auto k = fwd_chunked_kernel<T, VEC, MODE>;
     const int occ = occupancy(reinterpret_cast<const void *>(k), kThreads, 0);
     if (occ <= 0) return cudaErrorInvalidConfiguration;
     const int64_t cap = (int64_t)occ * sm_count;
     return launch_kernel(k, (unsigned)(a.M < cap ? a.M : cap), kThreads, 0, st, a);
 }
 
+template <typename T, int VEC>
+cudaError_t launch_mode(const FwdArgs &a, int mode, int sm_count, cudaStream_t st) {
+    switch (mode) {
+    case kPlain: return launch_t<T, VEC, kPlain>(a, sm_count, st);
+    case kResid: return launch_t<T, VEC, kResid>(a, sm_count, st);
+    case kAdaln: return launch_t<T, VEC, kAdaln>(a, sm_count, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
 template <typename T>
-cudaError_t launch_dt(const FwdArgs &a, bool vec, int sm_count, cudaStream_t st) {
+cudaError_t launch_dt(const FwdArgs &a, int mode, bool vec, int sm_count, cudaStream_t st) {
     constexpr int V = Vec16<T>::n;
-    const bool resid = a.r != nullptr;
-    if (vec) return resid ? launch_t<T, V, true>(a, sm_count, st) : launch_t<T, V, false>(a, sm_count, st);
-    return resid ? launch_t<T, 1, true>(a, sm_count, st) : launch_t<T, 1, false>(a, sm_count, st);
+    return vec ? launch_mode<T, V>(a, mode, sm_count, st) : launch_mode<T, 1>(a, mode, sm_count, st);
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_chunked(const FwdArgs &a, int dtype, bool vec, int sm_count, cudaStream_t st) {
+cudaError_t launch_fwd_chunked(const FwdArgs &a, int dtype, int mode, bool vec, int sm_count, cudaStream_t st) {
     switch (dtype) {
-    case kF32: return launch_dt<float>(a, vec, sm_count, st);
-    case kF16: return launch_dt<__half>(a, vec, sm_count, st);
-    case kBF16: return launch_dt<__nv_bfloat16>(a, vec, sm_count, st);
+    case kF32: return launch_dt<float>(a, mode, vec, sm_count, st);
+    case kF16: return launch_dt<__half>(a, mode, vec, sm_count, st);
+    case kBF16: return launch_dt<__nv_bfloat16>(a, mode, vec, sm_count, st);
     }
     return cudaErrorInvalidValue;
 }

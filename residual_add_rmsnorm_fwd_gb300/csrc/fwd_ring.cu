@@ -1,17 +1,19 @@
-// fwd_ring.cu -- RMSNorm forward (plain and residual-fused) with rows staged
-// in shared memory by bulk copies (TMA), for 16-byte aligned rows of LLM
-// hidden sizes.
+// fwd_ring.cu -- RMSNorm forward (plain, residual-fused, AdaLN) with rows
+// staged in shared memory by bulk copies (TMA), for 16-byte aligned rows of
+// LLM hidden sizes.
 //
 // Persistent grid: CTA b owns rows b, b + G, b + 2G, ...  A ring of NST
-// shared-memory stages, each holding one row of x (and one of the residual),
-// is kept full by one thread issuing cp.async.bulk copies whose completion is
-// counted by an mbarrier per stage.  So up to NST rows per CTA are in flight
-// from HBM while the CTA computes, independently of the register budget.
-// Each thread copies its NV 16-byte column groups from the stage into
-// registers, forms s = x (+ residual) in binary32 (two lanes per f32x2
-// instruction), writes residual_out, reduces sum(s^2) over the CTA, and
-// writes y = (s * rrms) * w from registers: the row is read from HBM once ("Skill: Write a Triton RMSNorm
-// Kernel", Required reasoning 3-10; Performance requirements).  The stage is
+// shared-memory stages, each holding one row of x (and of the residual, or
+// the row's AdaLN scale and shift), is kept full by one thread issuing
+// cp.async.bulk copies whose completion is counted by an mbarrier per stage.
+// So up to NST rows per CTA are in flight from HBM while the CTA computes,
+// independently of the register budget.  Each thread copies its NV 16-byte
+// column groups from the stage into registers, forms s = x (+ residual) in
+// binary32 (two lanes per f32x2 instruction), writes residual_out, reduces
+// sum(s^2) over the CTA, and writes y = (s * rrms) * w from registers: the
+// row is read from HBM once ("Skill: Write a Triton RMSNorm Kernel",
+// Required reasoning 3-10; Performance requirements).  AdaLN ("Rocm
+// Kernels" page, 4. AdaLN) continues y * (1 + scale) + shift.  The stage is
 // refilled with row k + NST as soon as the reduction barrier shows every
 // thread has copied it out.
 #include "bulk.cuh"
@@ -19,11 +21,13 @@
 
 namespace rmsn {
 
-template <typename T, int NV, bool RESID>
+template <typename T, int NV, int MODE>
 __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) {
+    constexpr bool RESID = MODE == kResid;
+    constexpr bool ADALN = MODE == kAdaln;
     constexpr int VEC = Vec16<T>::n;
-    constexpr int PR = Pairs16<T>::n;   // binary32 pairs per 16-byte group
-    constexpr int NS = RESID ? 2 : 1;   // streams staged per row
+    constexpr int PR = Pairs16<T>::n;                // binary32 pairs per 16-byte group
+    constexpr int NS = ADALN ? 3 : (RESID ? 2 : 1);  // rows staged per ring slot
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
@@ -33,6 +37,8 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
+    const T *__restrict__ scale = static_cast<const T *>(a.scale);
+    const T *__restrict__ shift = static_cast<const T *>(a.shift);
     T *__restrict__ y = static_cast<T *>(a.y);
     T *__restrict__ s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
@@ -44,10 +50,16 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     auto stage = [&](int s, int j) { return stages + (size_t)(s * NS + j) * rs.row_pitch; };
     auto issue = [&](int64_t k) {
         const int s = (int)(k % nst);
-        const int64_t base = (blockIdx.x + k * G) * a.stride;
+        const int64_t row = blockIdx.x + k * G;
+        const int64_t base = row * a.stride;
         mbar_arrive_expect_tx(&full[s], NS * rs.row_bytes);
         bulk_g2s(stage(s, 0), x + base, rs.row_bytes, &full[s]);
         if constexpr (RESID) bulk_g2s(stage(s, 1), r + base, rs.row_bytes, &full[s]);
+        if constexpr (ADALN) {
+            const int64_t cbase = (row / a.rows_per_cond) * a.cond_stride;
+            bulk_g2s(stage(s, 1), scale + cbase, rs.row_bytes, &full[s]);
+            bulk_g2s(stage(s, 2), shift + cbase, rs.row_bytes, &full[s]);
+        }
     };
 
     if (threadIdx.x == 0) {
@@ -76,6 +88,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
         // s = x (+ residual) in binary32, kept in registers for the scale step;
         // the post-add sum is written back as the next residual stream
         f32x2 sv[NV][PR];
+        P scp[NV], shp[NV];
         f32x2 ss2 = f2_make(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
@@ -88,6 +101,10 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
 #pragma unroll
                     for (int q = 0; q < PR; ++q) sv[i][q] = f2_add(sv[i][q], rv[q]);
                     st_global<T, VEC>(s_out + base + (int64_t)c * VEC, narrow16<T>(sv[i]));
+                }
+                if constexpr (ADALN) {   // out of the stage before the barrier frees it
+                    scp[i] = *reinterpret_cast<const P *>(stage(s, 1) + (size_t)c * 16);
+                    shp[i] = *reinterpret_cast<const P *>(stage(s, 2) + (size_t)c * 16);
                 }
 #pragma unroll
                 for (int q = 0; q < PR; ++q) ss2 = f2_fma(sv[i][q], sv[i][q], ss2);
@@ -112,6 +129,14 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                 f32x2 yv[PR];
 #pragma unroll
                 for (int q = 0; q < PR; ++q) yv[q] = f2_mul(f2_mul(sv[i][q], rr2), wv[i][q]);
+                if constexpr (ADALN) {   // y * (1 + scale) + shift
+                    f32x2 sc[PR], sh[PR];
+                    widen16<T>(scp[i], sc);
+                    widen16<T>(shp[i], sh);
+                    const f32x2 one2 = f2_make(1.0f, 1.0f);
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) yv[q] = f2_fma(yv[q], f2_add(one2, sc[q]), sh[q]);
+                }
                 st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(yv));
             }
         }
@@ -128,51 +153,68 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
 
 namespace {
 
-template <typename T, int NV, bool RESID>
+template <typename T, int NV, int MODE>
 cudaError_t launch_t(const FwdArgs &a, const RingPlan &p, cudaStream_t st) {
-    auto k = fwd_ring_kernel<T, NV, RESID>;
+    auto k = fwd_ring_kernel<T, NV, MODE>;
     cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(k), p.smem_bytes);
     if (e != cudaSuccess) return e;
     return launch_kernel(k, (unsigned)p.grid, (unsigned)p.threads, p.smem_bytes, st, a, p.shape);
 }
 
-template <typename T, bool RESID>
+// The ring geometry takes two or four 16-byte groups per thread.
+template <typename T, int MODE>
 const void *kernel_nv(int nv) {
     switch (nv) {
-    case 1: return reinterpret_cast<const void *>(fwd_ring_kernel<T, 1, RESID>);
-    case 2: return reinterpret_cast<const void *>(fwd_ring_kernel<T, 2, RESID>);
-    case 3: return reinterpret_cast<const void *>(fwd_ring_kernel<T, 3, RESID>);
-    case 4: return reinterpret_cast<const void *>(fwd_ring_kernel<T, 4, RESID>);
+    case 2: return reinterpret_cast<const void *>(fwd_ring_kernel<T, 2, MODE>);
+    case 4: return reinterpret_cast<const void *>(fwd_ring_kernel<T, 4, MODE>);
     }
     return nullptr;
 }
 
-const void *kernel_for(int dtype, bool resid, int nv) {
+template <typename T>
+const void *kernel_mode(int mode, int nv) {
+    switch (mode) {
+    case kPlain: return kernel_nv<T, kPlain>(nv);
+    case kResid: return kernel_nv<T, kResid>(nv);
+    case kAdaln: return kernel_nv<T, kAdaln>(nv);
+    }
+    return nullptr;
+}
+
+const void *kernel_for(int dtype, int mode, int nv) {
     switch (dtype) {
-    case kF32: return resid ? kernel_nv<float, true>(nv) : kernel_nv<float, false>(nv);
-    case kF16: return resid ? kernel_nv<__half, true>(nv) : kernel_nv<__half, false>(nv);
-    case kBF16: return resid ? kernel_nv<__nv_bfloat16, true>(nv) : kernel_nv<__nv_bfloat16, false>(nv);
+    case kF32: return kernel_mode<float>(mode, nv);
+    case kF16: return kernel_mode<__half>(mode, nv);
+    case kBF16: return kernel_mode<__nv_bfloat16>(mode, nv);
     }
     return nullptr;
 }
 
-template <typename T, bool RESID>
-cudaError_t launch_dt(const FwdArgs &a, const RingPlan &p, cudaStream_t st) {
+template <typename T, int MODE>
+cudaError_t launch_nv(const FwdArgs &a, const RingPlan &p, cudaStream_t st) {
     switch (p.nv) {
-    case 1: return launch_t<T, 1, RESID>(a, p, st);
-    case 2: return launch_t<T, 2, RESID>(a, p, st);
-    case 3: return launch_t<T, 3, RESID>(a, p, st);
-    case 4: return launch_t<T, 4, RESID>(a, p, st);
+    case 2: return launch_t<T, 2, MODE>(a, p, st);
+    case 4: return launch_t<T, 4, MODE>(a, p, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t launch_dt(const FwdArgs &a, int mode, const RingPlan &p, cudaStream_t st) {
+    switch (mode) {
+    case kPlain: return launch_nv<T, kPlain>(a, p, st);
+    case kResid: return launch_nv<T, kResid>(a, p, st);
+    case kAdaln: return launch_nv<T, kAdaln>(a, p, st);
     }
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-bool plan_fwd_ring(int64_t M, int H, int dtype, bool resid, int sm_count, RingPlan *out) {
+bool plan_fwd_ring(int64_t M, int H, int dtype, int mode, int sm_count, RingPlan *out) {
     RingPlan p{};
-    if (!fwd_ring_geometry(H, dtype, resid, &p)) return false;
-    const void *k = kernel_for(dtype, resid, p.nv);
+    if (!fwd_ring_geometry(H, dtype, mode, &p)) return false;
+    const void *k = kernel_for(dtype, mode, p.nv);
     if (k == nullptr || allow_dynamic_smem(k, p.smem_bytes) != cudaSuccess) return false;
     int occ = occupancy(k, p.threads, p.smem_bytes);
     if (occ <= 0) return false;
@@ -183,13 +225,11 @@ bool plan_fwd_ring(int64_t M, int H, int dtype, bool resid, int sm_count, RingPl
     return true;
 }
 
-cudaError_t launch_fwd_ring(const FwdArgs &a, int dtype, const RingPlan &p, cudaStream_t st) {
-    const bool resid = a.r != nullptr;
+cudaError_t launch_fwd_ring(const FwdArgs &a, int dtype, int mode, const RingPlan &p, cudaStream_t st) {
     switch (dtype) {
-    case kF32: return resid ? launch_dt<float, true>(a, p, st) : launch_dt<float, false>(a, p, st);
-    case kF16: return resid ? launch_dt<__half, true>(a, p, st) : launch_dt<__half, false>(a, p, st);
-    case kBF16:
-        return resid ? launch_dt<__nv_bfloat16, true>(a, p, st) : launch_dt<__nv_bfloat16, false>(a, p, st);
+    case kF32: return launch_dt<float>(a, mode, p, st);
+    case kF16: return launch_dt<__half>(a, mode, p, st);
+    case kBF16: return launch_dt<__nv_bfloat16>(a, mode, p, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -13,8 +13,10 @@
 
 namespace rmsn {
 
-template <typename T, int VEC, int NV, bool RESID, int U>
+template <typename T, int VEC, int NV, int MODE, int U>
 __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
+    constexpr bool RESID = MODE == kResid;
+    constexpr bool ADALN = MODE == kAdaln;
     using P = Pack<T, VEC>;
     // 16-byte groups compute on binary32 pairs (two-lane f32x2 instructions);
     // the scalar path (unaligned rows) one element at a time
@@ -24,6 +26,8 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
+    const T *__restrict__ scale = static_cast<const T *>(a.scale);
+    const T *__restrict__ shift = static_cast<const T *>(a.shift);
     T *__restrict__ y = static_cast<T *>(a.y);
     T *__restrict__ s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
@@ -44,17 +48,22 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
     int bank = 0;
     const int64_t groups = (a.M + U - 1) / U;
     for (int64_t grp = blockIdx.x; grp < groups; grp += gridDim.x) {
-        P xp[U][NV], rp[U][NV];
+        P xp[U][NV], rp[U][NV], scp[U][NV], shp[U][NV];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t row = grp * U + u;
             const int64_t base = row * a.stride;
+            const int64_t cbase = ADALN ? (row / a.rows_per_cond) * a.cond_stride : 0;
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 const int c = threadIdx.x + i * blockDim.x;
                 if (row < a.M && c < nvec) {
                     xp[u][i] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
                     if constexpr (RESID) rp[u][i] = ld_stream<T, VEC>(r + base + (int64_t)c * VEC);
+                    if constexpr (ADALN) {   // conditioning rows may be shared by many rows: cached path
+                        scp[u][i] = ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC);
+                        shp[u][i] = ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC);
+                    }
                 }
             }
         }
@@ -123,11 +132,21 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
                         widen16<T>(wp[i], wv);
 #pragma unroll
                         for (int q = 0; q < PR; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
+                        if constexpr (ADALN) {   // y * (1 + scale) + shift
+                            f32x2 sc[PR], sh[PR];
+                            widen16<T>(scp[u][i], sc);
+                            widen16<T>(shp[u][i], sh);
+                            const f32x2 one2 = f2_make(1.0f, 1.0f);
+#pragma unroll
+                            for (int q = 0; q < PR; ++q) sv[q] = f2_fma(sv[q], f2_add(one2, sc[q]), sh[q]);
+                        }
                         st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(sv));
                     } else {
                         float v = to_f32(xp[u][i].v[0]);
                         if constexpr (RESID) v += to_f32(rp[u][i].v[0]);
-                        y[base + c] = from_f32<T>((v * rrms) * to_f32(wp[i].v[0]));
+                        v = (v * rrms) * to_f32(wp[i].v[0]);
+                        if constexpr (ADALN) v = fmaf(v, 1.0f + to_f32(scp[u][i].v[0]), to_f32(shp[u][i].v[0]));
+                        y[base + c] = from_f32<T>(v);
                     }
                 }
             }
@@ -162,9 +181,9 @@ bool pick(int nvec, bool vec, int &threads, int &nv) {
     return false;
 }
 
-template <typename T, int VEC, int NV, bool RESID, int U>
+template <typename T, int VEC, int NV, int MODE, int U>
 cudaError_t launch_u(const FwdArgs &a, int threads, int64_t grid, cudaStream_t st) {
-    return launch_kernel(fwd_row_kernel<T, VEC, NV, RESID, U>, (unsigned)grid, (unsigned)threads, 0, st, a);
+    return launch_kernel(fwd_row_kernel<T, VEC, NV, MODE, U>, (unsigned)grid, (unsigned)threads, 0, st, a);
 }
 
 // Rows per pass: 2 keeps twice the bytes in flight per thread, but the rows
@@ -173,9 +192,9 @@ cudaError_t launch_u(const FwdArgs &a, int threads, int64_t grid, cudaStream_t s
 // rows of work for the slowest CTA instead of nine).  Take 2 only for
 // vector rows of at most 4 KB and only when it does not lengthen the
 // slowest CTA's share.
-template <typename T, int VEC, int NV, bool RESID>
+template <typename T, int VEC, int NV, int MODE>
 cudaError_t launch_t(const FwdArgs &a, int threads, int sm_count, cudaStream_t st) {
-    const int occ = occupancy(reinterpret_cast<const void *>(fwd_row_kernel<T, VEC, NV, RESID, 1>), threads, 0);
+    const int occ = occupancy(reinterpret_cast<const void *>(fwd_row_kernel<T, VEC, NV, MODE, 1>), threads, 0);
     if (occ <= 0) return cudaErrorInvalidConfiguration;
     const int64_t cap = (int64_t)occ * sm_count;
     auto share = [&](int64_t u) {   // rows handled by the busiest CTA
@@ -185,49 +204,54 @@ cudaError_t launch_t(const FwdArgs &a, int threads, int sm_count, cudaStream_t s
     if constexpr (VEC > 1 && NV <= 2) {
         if (share(2) <= share(1)) {
             const int occ2 =
-                occupancy(reinterpret_cast<const void *>(fwd_row_kernel<T, VEC, NV, RESID, 2>), threads, 0);
+                occupancy(reinterpret_cast<const void *>(fwd_row_kernel<T, VEC, NV, MODE, 2>), threads, 0);
             if (occ2 >= occ) {
                 const int64_t groups = (a.M + 1) / 2;
-                return launch_u<T, VEC, NV, RESID, 2>(a, threads, groups < cap ? groups : cap, st);
+                return launch_u<T, VEC, NV, MODE, 2>(a, threads, groups < cap ? groups : cap, st);
             }
         }
     }
-    return launch_u<T, VEC, NV, RESID, 1>(a, threads, a.M < cap ? a.M : cap, st);
+    return launch_u<T, VEC, NV, MODE, 1>(a, threads, a.M < cap ? a.M : cap, st);
 }
 
-template <typename T, int VEC, bool RESID>
+template <typename T, int VEC, int MODE>
 cudaError_t launch_nv(const FwdArgs &a, int nv, int threads, int sm_count, cudaStream_t st) {
     if constexpr (VEC > 1) {
         switch (nv) {
-        case 1: return launch_t<T, VEC, 1, RESID>(a, threads, sm_count, st);
-        case 2: return launch_t<T, VEC, 2, RESID>(a, threads, sm_count, st);
-        case 3: return launch_t<T, VEC, 3, RESID>(a, threads, sm_count, st);
-        case 4: return launch_t<T, VEC, 4, RESID>(a, threads, sm_count, st);
+        case 1: return launch_t<T, VEC, 1, MODE>(a, threads, sm_count, st);
+        case 2: return launch_t<T, VEC, 2, MODE>(a, threads, sm_count, st);
+        case 3: return launch_t<T, VEC, 3, MODE>(a, threads, sm_count, st);
+        case 4: return launch_t<T, VEC, 4, MODE>(a, threads, sm_count, st);
         }
     } else {
         switch (nv) {
-        case 1: return launch_t<T, 1, 1, RESID>(a, threads, sm_count, st);
-        case 2: return launch_t<T, 1, 2, RESID>(a, threads, sm_count, st);
-        case 4: return launch_t<T, 1, 4, RESID>(a, threads, sm_count, st);
-        case 8: return launch_t<T, 1, 8, RESID>(a, threads, sm_count, st);
-        case 16: return launch_t<T, 1, 16, RESID>(a, threads, sm_count, st);
+        case 1: return launch_t<T, 1, 1, MODE>(a, threads, sm_count, st);
+        case 2: return launch_t<T, 1, 2, MODE>(a, threads, sm_count, st);
+        case 4: return launch_t<T, 1, 4, MODE>(a, threads, sm_count, st);
+        case 8: return launch_t<T, 1, 8, MODE>(a, threads, sm_count, st);
+        case 16: return launch_t<T, 1, 16, MODE>(a, threads, sm_count, st);
         }
     }
     return cudaErrorInvalidValue;
 }
 
+template <typename T, int VEC>
+cudaError_t launch_mode(const FwdArgs &a, int mode, int nv, int threads, int sm_count, cudaStream_t st) {
+    switch (mode) {
+    case kPlain: return launch_nv<T, VEC, kPlain>(a, nv, threads, sm_count, st);
+    case kResid: return launch_nv<T, VEC, kResid>(a, nv, threads, sm_count, st);
+    case kAdaln: return launch_nv<T, VEC, kAdaln>(a, nv, threads, sm_count, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
 template <typename T>
-cudaError_t launch_dt(const FwdArgs &a, bool vec, int sm_count, cudaStream_t st) {
+cudaError_t launch_dt(const FwdArgs &a, int mode, bool vec, int sm_count, cudaStream_t st) {
     constexpr int V = Vec16<T>::n;
     int threads = 0, nv = 0;
     if (!pick(vec ? a.H / V : a.H, vec, threads, nv)) return cudaErrorInvalidValue;
-    const bool resid = a.r != nullptr;
-    if (vec) {
-        return resid ? launch_nv<T, V, true>(a, nv, threads, sm_count, st)
-                     : launch_nv<T, V, false>(a, nv, threads, sm_count, st);
-    }
-    return resid ? launch_nv<T, 1, true>(a, nv, threads, sm_count, st)
-                 : launch_nv<T, 1, false>(a, nv, threads, sm_count, st);
+    return vec ? launch_mode<T, V>(a, mode, nv, threads, sm_count, st)
+               : launch_mode<T, 1>(a, mode, nv, threads, sm_count, st);
 }
 
 }  // namespace
@@ -237,11 +261,11 @@ bool fwd_row_fits(int H, int dtype, bool vec) {
     return pick(vec ? H / vec_elems(dtype) : H, vec, threads, nv);
 }
 
-cudaError_t launch_fwd_row(const FwdArgs &a, int dtype, bool vec, int sm_count, cudaStream_t st) {
+cudaError_t launch_fwd_row(const FwdArgs &a, int dtype, int mode, bool vec, int sm_count, cudaStream_t st) {
     switch (dtype) {
-    case kF32: return launch_dt<float>(a, vec, sm_count, st);
-    case kF16: return launch_dt<__half>(a, vec, sm_count, st);
-    case kBF16: return launch_dt<__nv_bfloat16>(a, vec, sm_count, st);
+    case kF32: return launch_dt<float>(a, mode, vec, sm_count, st);
+    case kF16: return launch_dt<__half>(a, mode, vec, sm_count, st);
+    case kBF16: return launch_dt<__nv_bfloat16>(a, mode, vec, sm_count, st);
     }
     return cudaErrorInvalidValue;
 }

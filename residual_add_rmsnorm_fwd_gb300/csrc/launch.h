@@ -45,22 +45,24 @@ struct RingPlan {
 
 // Ring shapes measured best on GB300 (see the kernel files): false when the
 // row is too short to profit from the ring or too long for it.
-bool fwd_ring_geometry(int H, int dtype, bool resid, RingPlan *p);
+bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p);
 bool bwd_ring_geometry(int H, int dtype, bool dres, RingPlan *p);
 
+// Forward launchers take the FwdMode (plain, residual-fused, AdaLN).
 // Forward with rows staged by bulk copies (16-byte aligned rows only).
-bool plan_fwd_ring(int64_t M, int H, int dtype, bool resid, int sm_count, RingPlan *out);
-cudaError_t launch_fwd_ring(const FwdArgs &a, int dtype, const RingPlan &p, cudaStream_t st);
+bool plan_fwd_ring(int64_t M, int H, int dtype, int mode, int sm_count, RingPlan *out);
+cudaError_t launch_fwd_ring(const FwdArgs &a, int dtype, int mode, const RingPlan &p, cudaStream_t st);
 
-// Small H (below 256): a warp, or an aligned group of 1..32 lanes, per row.
+// Small H (below 256): a warp, or an aligned group of 1..32 lanes, per row
+// (plain and residual-fused only; a.r selects the fused form).
 cudaError_t launch_fwd_small(const FwdArgs &a, int dtype, bool vec, int sm_count, cudaStream_t st);
 
 // Row kept in registers between the sum of squares and the scale step.
 bool fwd_row_fits(int H, int dtype, bool vec);
-cudaError_t launch_fwd_row(const FwdArgs &a, int dtype, bool vec, int sm_count, cudaStream_t st);
+cudaError_t launch_fwd_row(const FwdArgs &a, int dtype, int mode, bool vec, int sm_count, cudaStream_t st);
 
 // H above the register budget: two passes over the row in chunks.
-cudaError_t launch_fwd_chunked(const FwdArgs &a, int dtype, bool vec, int sm_count, cudaStream_t st);
+cudaError_t launch_fwd_chunked(const FwdArgs &a, int dtype, int mode, bool vec, int sm_count, cudaStream_t st);
 
 // Backward: dx per row plus per-CTA dweight partials, then the fixed-order
 // column reduction of the partials.

@@ -104,3 +104,19 @@ def check_dweight(got: np.ndarray, ref: np.ndarray, ref_abs: np.ndarray, rtol: f
 
 def bwd_rtol(dtype: str) -> float:
     return 1e-5 if dtype == "f32" else 2e-2
+
+
+def check_adaln_values(got_bits: np.ndarray, ref64: np.ndarray, y_scale: np.ndarray, dtype: str, oracle) -> dict:
+    """AdaLN tolerance per element.  y = t + shift can cancel, so the binary32
+    evaluation error is relative to y_scale = |t| + |shift|, not to |y|:
+    fp32 within 1e-5 * y_scale; f16/bf16 within 1 ulp of the oracle's value
+    rounded to the storage type, or within 1e-5 * y_scale of it."""
+    got = oracle.decode(got_bits, dtype)
+    err = np.abs(got - ref64)
+    ok = err <= 1e-5 * y_scale
+    if dtype != "f32":
+        want = oracle.encode(ref64, dtype)
+        ok |= np.abs(ordinal(got_bits) - ordinal(want)) <= 1
+    bad = ~ok
+    rel = err / np.where(y_scale > 0, y_scale, 1)
+    return {"failed": int(bad.sum()), "max_rel": float(rel.max()) if rel.size else 0.0, "bad": bad}

@@ -155,3 +155,44 @@ def test_bwd_residual_invalid(lib):
     assert bwd(dr=None) == INVALID
     assert bwd(dr=R + 1) == INVALID
     assert bwd(M=0, dr=None, dw=None) == OK
+
+
+SC, SH = 0x700000, 0x800000
+
+
+def adaln(lib, **kw):
+    a = dict(x=X, w=W, sc=SC, sh=SH, y=Y, rrms=Q, stride=64, cs=64, rpc=1, M=4, H=64, eps=1e-6, dtype=2,
+             has_w=1)
+    a.update(kw)
+    return lib.rmsnorm_adaln_fwd(a["x"], a["w"], a["sc"], a["sh"], a["y"], a["rrms"], a["stride"], a["cs"],
+                                 a["rpc"], a["M"], a["H"], a["eps"], a["dtype"], a["has_w"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(sc=None), dict(sh=None), dict(x=None), dict(y=None), dict(w=None), dict(rpc=0), dict(rpc=-2),
+    dict(cs=63), dict(sc=SC + 1), dict(sh=SH + 1), dict(eps=-1.0), dict(dtype=5), dict(stride=32),
+    dict(cs=1 << 60, M=5, rpc=1),
+])
+def test_adaln_invalid(lib, kw):
+    assert adaln(lib, **kw) == INVALID
+
+
+@pytest.mark.parametrize("kw", [
+    dict(y=SC), dict(y=SH + 2 * 64 * 2), dict(rrms=SC + 16), dict(y=X + 2), dict(y=W),
+    # with 2 rows per conditioning row, scale holds rows 0..1 only: row 1 of it still overlaps y
+    dict(rpc=2, y=SC + 64 * 2),
+])
+def test_adaln_alias(lib, kw):
+    assert adaln(lib, **kw) == ALIAS
+
+
+def test_adaln_conditioning_extent(lib):
+    # M = 4 rows, 2 per conditioning row: scale spans 2 rows (256 bytes in bf16), so y right after it
+    # passes validation (the call then needs a device: no GPU here, so it stops there)
+    passed = lambda st: st not in (INVALID, ALIAS)
+    assert passed(adaln(lib, rpc=2, y=SC + 2 * 64 * 2))
+    assert passed(adaln(lib, rpc=4, sh=SC + 64 * 2))   # one conditioning row each; inputs may overlap
+    assert passed(adaln(lib, y=X))                     # in place
+    assert adaln(lib, rpc=2, y=SC + 2 * 64 * 2 - 2) == ALIAS
+    assert adaln(lib, sc=None, sh=None, x=None, y=None, M=0) == OK
+    assert adaln(lib, w=None, has_w=0, M=0) == OK

@@ -88,6 +88,20 @@ def matrix(rng, M: int, H: int, dtype: str, stride: int | None = None,
     return out.view(STORAGE[dtype])
 
 
+def conditioning(rng, n: int, H: int, dtype: str, stride: int | None = None, sigma: float = 0.5) -> np.ndarray:
+    """An (n, stride) storage array of AdaLN conditioning rows (scale or
+    shift): sigma * N(0, 1) in the first H columns, sentinels in the padding.
+    (In a DiT block these come out of the timestep-embedding MLP; zero-mean
+    values of moderate size stand in for them.)"""
+    stride = H if stride is None else stride
+    body = to_storage(sigma * rng.standard_normal((n, H), dtype=np.float32), dtype)
+    if stride == H:
+        return body
+    out = sentinel_fill((n, stride), dtype)
+    out.view(body.dtype)[:, :H] = body
+    return out.view(STORAGE[dtype])
+
+
 def weight(rng, H: int, dtype: str) -> np.ndarray:
     """1 + 0.1 * N(0, 1), rounded to the storage format."""
     return to_storage(1.0 + 0.1 * rng.standard_normal(H, dtype=np.float32), dtype)
