@@ -3,7 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                     [--workload step|fused_fwd|fused_fwd_bwd_residual|dit_mix|fwd_f32_small|
-                                fwd_bwd_8192|fused_f16_padded]
+                                fwd_bwd_8192|fused_f16_padded|adaln|adaln_per_token]
 
 Default workload ("step"): one pass of the whole hot path on the
 (B=8, T=2048, H=4096) bf16 activations, M = 16384 rows -- the fused
@@ -395,13 +395,13 @@ class AdalnWorkload:
     """AdaLN forward of a DiT block: y = norm(x) * w * (1 + scale) + shift on
     2 sequences x 6144 tokens x 2048 bf16 (the video-DiT token shape of the
     168-call mix), one conditioning row per sequence broadcast over its
-    tokens.  Eight calls per step over four rotating x/y buffer sets, so that
-    no call finds its operands in L2."""
-    name = "adaln_bf16_2x6144x2048_per_sequence"
+    tokens (``per_token``: one conditioning row per token, scale and shift
+    as large as x).  Eight calls per step over four rotating buffer sets, so
+    that no call finds its operands in L2."""
     flush_l2 = False
     n_calls, n_sets = 8, 4
 
-    def __init__(self):
+    def __init__(self, per_token=False):
         import torch
         import residual_add_rmsnorm_fwd_gb300 as rn
         import workloads as wl
@@ -409,12 +409,17 @@ class AdalnWorkload:
         self.B, self.T, self.H, self.dt, self.eps = 2, 6144, 2048, "bf16", 1e-6
         self.M, self.S = self.B * self.T, self.H
         self.es = wl.ELEM_BYTES[self.dt]
-        rng = wl.rng_for(40)
+        self.per_token = per_token
+        self.rpc = 1 if per_token else self.T
+        self.n_cond = self.M // self.rpc
+        self.name = f"adaln_bf16_2x6144x2048_per_{'token' if per_token else 'sequence'}"
+        rng = wl.rng_for(41 if per_token else 40)
         self.host = {"xs": [wl.matrix(rng, self.M, self.H, self.dt) for _ in range(self.n_sets)],
-                     "w": wl.weight(rng, self.H, self.dt),
-                     "scale": wl.conditioning(rng, self.B, self.H, self.dt),
-                     "shift": wl.conditioning(rng, self.B, self.H, self.dt)}
-        self.call_bytes = 2 * self.M * self.H * self.es + 3 * self.B * self.H * self.es + self.H * self.es
+                     "w": wl.weight(rng, self.H, self.dt)}
+        n_cond_sets = self.n_sets if per_token else 1
+        self.host["scales"] = [wl.conditioning(rng, self.n_cond, self.H, self.dt) for _ in range(n_cond_sets)]
+        self.host["shifts"] = [wl.conditioning(rng, self.n_cond, self.H, self.dt) for _ in range(n_cond_sets)]
+        self.call_bytes = (2 * self.M * self.H + 2 * self.n_cond * self.H + self.H) * self.es
         self.bytes_per_step = self.n_calls * self.call_bytes
         self.rows_per_step = self.n_calls * self.M
         self.kernels_per_step = self.n_calls
@@ -424,32 +429,33 @@ class AdalnWorkload:
         torch, wl, dt = self.torch, self.wl, self.dt
         dev = torch.device("cuda")
         b = SimpleNamespace()
-        b.xs = [wl.to_torch(a, dt).to(dev) for a in self.host["xs"]]
+        up = lambda a: wl.to_torch(a, dt).to(dev)  # noqa: E731
+        b.xs = [up(a) for a in self.host["xs"]]
         b.ys = [torch.empty_like(x) for x in b.xs]
+        b.scs = [up(a) for a in self.host["scales"]]
+        b.shs = [up(a) for a in self.host["shifts"]]
         return b
 
     def setup(self):
-        dev = self.torch.device("cuda")
-        up = lambda a: self.wl.to_torch(a, self.dt).to(dev)  # noqa: E731
-        self.w, self.sc, self.sh = up(self.host["w"]), up(self.host["scale"]), up(self.host["shift"])
+        self.w = self.wl.to_torch(self.host["w"], self.dt).to(self.torch.device("cuda"))
         self.sets = [self._make_set()]
         return self
 
     def calls(self, k=0):
-        rn, b = self.rn, self.sets[k]
-        return [("adaln", lambda x=b.xs[i % self.n_sets], y=b.ys[i % self.n_sets]: rn.rmsnorm_adaln_fwd(
-                    x, self.w, self.sc, self.sh, y, rows_per_cond=self.T, eps=self.eps), self.call_bytes)
+        rn, b, n = self.rn, self.sets[k], self.n_sets
+        return [("adaln", lambda x=b.xs[i % n], y=b.ys[i % n], sc=b.scs[i % len(b.scs)], sh=b.shs[i % len(b.shs)]:
+                 rn.rmsnorm_adaln_fwd(x, self.w, sc, sh, y, rows_per_cond=self.rpc, eps=self.eps), self.call_bytes)
                 for i in range(self.n_calls)]
 
     def config(self):
         return {"workload": self.name, "M": self.M, "H": self.H, "B": self.B, "T": self.T, "dtype": self.dt,
-                "rows_per_cond": self.T, "calls_per_step": self.n_calls, "eps": self.eps,
-                "l2": f"{self.n_sets} rotating x/y buffer sets of {2 * self.M * self.H * self.es} bytes",
+                "rows_per_cond": self.rpc, "calls_per_step": self.n_calls, "eps": self.eps,
+                "l2": f"{self.n_sets} rotating buffer sets of {self.call_bytes} bytes",
                 "algorithmic_bytes_per_step": self.bytes_per_step}
 
     def e2e_setup(self):
         torch, b = self.torch, self.sets[0]
-        self.h_in = [x.cpu().pin_memory() for x in b.xs]
+        self.h_in = [t.cpu().pin_memory() for t in b.xs + b.scs + b.shs]
         self.h_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in b.ys]
         while len(self.sets) < 2:
             self.sets.append(self._make_set())
@@ -458,12 +464,13 @@ class AdalnWorkload:
 
     def e2e_transfers(self, k):
         b = self.sets[k]
-        return list(zip(b.xs, self.h_in)), list(zip(self.h_out, b.ys))
+        return list(zip(b.xs + b.scs + b.shs, self.h_in)), list(zip(self.h_out, b.ys))
 
     def oracle_step(self, rows):
         import oracle
-        oracle.rmsnorm_adaln_fwd(self.host["xs"][0][:rows], self.host["w"], self.host["scale"][:1],
-                                 self.host["shift"][:1], self.eps, self.dt, rows_per_cond=self.T)
+        n = -(-rows // self.rpc)
+        oracle.rmsnorm_adaln_fwd(self.host["xs"][0][:rows], self.host["w"], self.host["scales"][0][:n],
+                                 self.host["shifts"][0][:n], self.eps, self.dt, rows_per_cond=self.rpc)
         return rows * self.call_bytes / self.M
 
 
@@ -482,6 +489,7 @@ WORKLOADS = {
     "fwd_f32_small": SmallFwdWorkload,
     "dit_mix": DitMixWorkload,
     "adaln": AdalnWorkload,
+    "adaln_per_token": lambda: AdalnWorkload(per_token=True),
     "step": lambda: StepWorkload(2, backward=True),
     "fused_fwd": lambda: StepWorkload(2, backward=False),
     "fused_fwd_bwd_residual": lambda: StepWorkload(2, backward=True, dres=True),

@@ -112,13 +112,20 @@ bool rows_vectorisable(int64_t H, int64_t stride, int dtype) {
 int to_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA; }
 
 // Kernel family by row length and layout: lane groups below 256 elements
-// (plain and residual-fused; AdaLN takes the register kernel there), the
-// bulk-copy ring for aligned rows of at least 8 KB, the register kernel, and
-// the two-pass chunked kernel above the register budget.
+// (plain and residual-fused; AdaLN takes the register kernel there), a warp
+// per aligned row of 512 B to 2 KB (plain, and AdaLN whose conditioning rows
+// are each shared by at least 8 rows), the bulk-copy ring for aligned rows
+// of at least 8 KB, the register kernel, and the two-pass chunked kernel
+// above the register budget.
 int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, int sms, cudaStream_t s) {
     if (a.H < kSmallH && mode != kAdaln) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
+    const bool shared_cond = mode == kAdaln && a.rows_per_cond >= 8;
+    if (vec && (mode == kPlain || shared_cond) && fwd_warp_fits(a.H, dtype))
+        return to_status(launch_fwd_warp(a, dtype, mode, sms, s));
     RingPlan ring;
-    if (vec && plan_fwd_ring(a.M, a.H, dtype, mode, sms, &ring)) return to_status(launch_fwd_ring(a, dtype, mode, ring, s));
+    const int ring_mode = shared_cond ? kAdalnShared : mode;
+    if (vec && plan_fwd_ring(a.M, a.H, dtype, ring_mode, sms, &ring))
+        return to_status(launch_fwd_ring(a, dtype, ring_mode, ring, s));
     if (fwd_row_fits(a.H, dtype, vec)) return to_status(launch_fwd_row(a, dtype, mode, vec, sms, s));
     return to_status(launch_fwd_chunked(a, dtype, mode, vec, sms, s));
 }
@@ -238,7 +245,7 @@ int adaln_forward(const void *x, const void *weight, const void *scale, const vo
     a.scale = scale;
     a.shift = shift;
     a.cond_stride = cond_stride;
-    a.rows_per_cond = rows_per_cond;
+    a.rows_per_cond = rows_per_cond < M ? rows_per_cond : M;   // below 2^31, like M: 32-bit division
     return dispatch_fwd(a, dtype, kAdaln, vec, sms, static_cast<cudaStream_t>(stream));
 }
 
@@ -279,9 +286,15 @@ void finish_ring(RingPlan *p, int nv, int threads, int64_t row_bytes, int stream
 }  // namespace
 
 // Forward: rows of at least 8 KB.  Two 16-byte groups per thread (four above
-// 1024 groups), two stages, two CTAs per SM: measured best at H = 4096-8192
-// (deeper rings or more CTAs per SM put more rows in flight and lose DRAM
-// efficiency); shorter rows run faster on the register kernel.
+// 1024 groups).  Measured on GB300 at H = 4096-8192:
+//   - residual-fused (two input rows per slot): two stages, two CTAs per
+//     SM; deeper rings or more CTAs per SM put more rows in flight and lose
+//     DRAM efficiency;
+//   - one input row per slot (plain, and AdaLN with shared conditioning
+//     rows): up to four CTAs per SM, two stages (three above 12 KB rows):
+//     plain bf16 H = 4096, 4862 -> 6185 GB/s against two CTAs; H = 8192,
+//     5907 -> 6305 GB/s with the third stage.
+// Shorter rows run faster on the register and warp kernels.
 bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
     const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
     if (row_bytes % 16 != 0 || row_bytes < 8192) return false;
@@ -290,9 +303,10 @@ bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
     const int threads = round_up_to(ceil_div(nvec, nv), 32);
     if (threads > 512) return false;
     const int streams = mode == kAdaln ? 3 : (mode == kResid ? 2 : 1);   // x (+ residual | scale, shift)
-    const int stages = 2;
+    const bool plain = streams == 1;   // plain, or AdaLN reading shared conditioning rows through L1
+    const int stages = plain && row_bytes > 12288 ? 3 : 2;
     if (kRingHeaderBytes + (size_t)stages * streams * round_up_to((int)row_bytes, 128) > 200 * 1024) return false;
-    finish_ring(p, nv, threads, row_bytes, streams, stages, 2);
+    finish_ring(p, nv, threads, row_bytes, streams, stages, plain ? 4 : 2);
     return true;
 }
 

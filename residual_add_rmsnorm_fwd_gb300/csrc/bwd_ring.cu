@@ -43,8 +43,7 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
     const int64_t nrows = (a.M - 1 - blockIdx.x) / G + 1;  // the grid never exceeds M
 
     auto stage = [&](int s, int j) { return stages + (size_t)(s * NS + j) * rs.row_pitch; };
-    auto issue = [&](int64_t k) {
-        const int s = (int)(k % nst);
+    auto issue = [&](int64_t k, int s) {   // row k of this CTA into stage s (= k mod nst)
         const int64_t base = (blockIdx.x + k * G) * a.stride;
         mbar_arrive_expect_tx(&full[s], NS * rs.row_bytes);
         bulk_g2s(stage(s, 0), dy + base, rs.row_bytes, &full[s]);
@@ -58,7 +57,7 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
     }
     __syncthreads();
     if (threadIdx.x == 0)
-        for (int64_t k = 0; k < nst && k < nrows; ++k) issue(k);
+        for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
     P wp[NV];
     f32x2 acc[NV][PR];
@@ -74,12 +73,16 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
     bool gave_up = false;
     float rr_next = __ldg(a.rrms + blockIdx.x);
     for (int64_t k = 0; k < nrows; ++k) {
-        const int s = (int)(k % nst);
+        // stage s = k mod nst and its mbarrier phase (k / nst) mod 2, in 32
+        // bits (rows per CTA < 2^31); a stage counter advanced per row, as in
+        // the forward ring, measured slower here (ptxas spilled)
+        const int s = (int)((uint32_t)k % (uint32_t)nst);
+        const uint32_t phase = ((uint32_t)k / (uint32_t)nst) & 1u;
         const int64_t base = (blockIdx.x + k * G) * a.stride;
         const float rr = rr_next;
         if (k + 1 < nrows) rr_next = __ldg(a.rrms + blockIdx.x + (k + 1) * G);
         const f32x2 rr2 = f2_make(rr, rr);
-        if (!mbar_wait_bounded(&full[s], (uint32_t)((k / nst) & 1), a.err)) gave_up = true;
+        if (!mbar_wait_bounded(&full[s], phase, a.err)) gave_up = true;
 
         P gp[NV], xp[NV], rp[NV];
         f32x2 dot2 = f2_make(0.0f, 0.0f);
@@ -107,7 +110,7 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
             fence_proxy_async_smem();
-            issue(k + nst);
+            issue(k + nst, s);
         }
         const f32x2 nc2 = f2_make(-c_row, -c_row);
 #pragma unroll
@@ -149,9 +152,9 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
         }
     }
     if (gave_up && threadIdx.x == 0) {
-        for (int s = 0; s < nst && s < nrows; ++s) {
-            const int64_t uses = (nrows - 1 - s) / nst + 1;
-            mbar_wait_bounded(&full[s], (uint32_t)((uses - 1) & 1), nullptr);
+        for (int j = 0; j < nst && j < nrows; ++j) {
+            const int64_t uses = (nrows - 1 - j) / nst + 1;
+            mbar_wait_bounded(&full[j], (uint32_t)((uses - 1) & 1), nullptr);
         }
     }
 }

@@ -32,11 +32,15 @@ struct FwdArgs {
     const void *scale;
     const void *shift;
     int64_t cond_stride;
-    int64_t rows_per_cond;
+    int64_t rows_per_cond;   // 1..M (clamped to M by the host), so row / rows_per_cond fits 32 bits
 };
 
-// Forward variants: plain norm, residual-fused, AdaLN (norm * w * (1 + scale) + shift).
-enum FwdMode { kPlain = 0, kResid = 1, kAdaln = 2 };
+// Forward variants: plain norm, residual-fused, AdaLN (norm * w * (1 + scale)
+// + shift).  kAdalnShared is AdaLN whose conditioning rows are each shared
+// by many rows: the bulk-copy ring then reads them through L1 instead of
+// staging a copy per row (every SM copying the same few rows from L2 makes
+// those L2 lines a hot spot); the other kernels read them through L1 always.
+enum FwdMode { kPlain = 0, kResid = 1, kAdaln = 2, kAdalnShared = 3 };
 
 struct BwdArgs {
     const void *dy;

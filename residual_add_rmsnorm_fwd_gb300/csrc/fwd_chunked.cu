@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
     int bank = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * a.stride;
-        const int64_t cbase = ADALN ? (row / a.rows_per_cond) * a.cond_stride : 0;
+        const int64_t cbase = ADALN ? (int64_t)((uint32_t)row / (uint32_t)a.rows_per_cond) * a.cond_stride : 0;
         float ss = 0.0f;
         for (int c0 = 0; c0 < nvec; c0 += chunk) {
             P xp[U], rp[U];

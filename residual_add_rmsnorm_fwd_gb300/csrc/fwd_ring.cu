@@ -13,9 +13,13 @@
 // sum(s^2) over the CTA, and writes y = (s * rrms) * w from registers: the
 // row is read from HBM once ("Skill: Write a Triton RMSNorm Kernel",
 // Required reasoning 3-10; Performance requirements).  AdaLN ("Rocm
-// Kernels" page, 4. AdaLN) continues y * (1 + scale) + shift.  The stage is
-// refilled with row k + NST as soon as the reduction barrier shows every
-// thread has copied it out.
+// Kernels" page, 4. AdaLN) continues y * (1 + scale) + shift: per-token
+// conditioning rows are staged beside x; conditioning rows shared by many
+// rows (one per sequence) are read through L1 only when the CTA's row moves
+// to another one, and kept as w * (1 + scale) and shift in registers, so a
+// row costs one fused multiply-add per element more than the plain norm.
+// The stage is refilled with row k + NST as soon as the reduction barrier
+// shows every thread has copied it out.
 #include "bulk.cuh"
 #include "launch.h"
 
@@ -24,10 +28,11 @@ namespace rmsn {
 template <typename T, int NV, int MODE>
 __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) {
     constexpr bool RESID = MODE == kResid;
-    constexpr bool ADALN = MODE == kAdaln;
+    constexpr bool ADALN = MODE == kAdaln || MODE == kAdalnShared;
+    constexpr bool STAGE_COND = MODE == kAdaln;           // scale/shift rows staged beside x
     constexpr int VEC = Vec16<T>::n;
-    constexpr int PR = Pairs16<T>::n;                // binary32 pairs per 16-byte group
-    constexpr int NS = ADALN ? 3 : (RESID ? 2 : 1);  // rows staged per ring slot
+    constexpr int PR = Pairs16<T>::n;                     // binary32 pairs per 16-byte group
+    constexpr int NS = STAGE_COND ? 3 : (RESID ? 2 : 1);  // rows staged per ring slot
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
@@ -48,15 +53,14 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     const int64_t nrows = (a.M - 1 - blockIdx.x) / G + 1;  // the grid never exceeds M
 
     auto stage = [&](int s, int j) { return stages + (size_t)(s * NS + j) * rs.row_pitch; };
-    auto issue = [&](int64_t k) {
-        const int s = (int)(k % nst);
+    auto issue = [&](int64_t k, int s) {   // row k of this CTA into stage s (= k mod nst)
         const int64_t row = blockIdx.x + k * G;
         const int64_t base = row * a.stride;
         mbar_arrive_expect_tx(&full[s], NS * rs.row_bytes);
         bulk_g2s(stage(s, 0), x + base, rs.row_bytes, &full[s]);
         if constexpr (RESID) bulk_g2s(stage(s, 1), r + base, rs.row_bytes, &full[s]);
-        if constexpr (ADALN) {
-            const int64_t cbase = (row / a.rows_per_cond) * a.cond_stride;
+        if constexpr (STAGE_COND) {
+            const int64_t cbase = (int64_t)((uint32_t)row / (uint32_t)a.rows_per_cond) * a.cond_stride;
             bulk_g2s(stage(s, 1), scale + cbase, rs.row_bytes, &full[s]);
             bulk_g2s(stage(s, 2), shift + cbase, rs.row_bytes, &full[s]);
         }
@@ -68,22 +72,54 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     }
     __syncthreads();
     if (threadIdx.x == 0)
-        for (int64_t k = 0; k < nst && k < nrows; ++k) issue(k);
+        for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
-    // weight (H,), by column only, widened once per CTA; ones without weight
+    // weight (H,), by column only, widened once per CTA; ones without weight.
+    // With shared conditioning rows wv holds w * (1 + scale) of the current
+    // conditioning row instead, and shc its shift: refreshed only when the
+    // CTA's next row belongs to another conditioning row.
     f32x2 wv[NV][PR];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
+    auto load_w = [&](int i) {
         const int c = threadIdx.x + i * blockDim.x;
-        widen16<T>((a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>()), wv[i]);
+        return (a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+    };
+    if constexpr (MODE != kAdalnShared) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) widen16<T>(load_w(i), wv[i]);
     }
+    P shc[NV];
+    uint32_t c_cur = 0xffffffffu;
 
     int bank = 0;
     bool gave_up = false;
+    // stage s = k mod nst and its mbarrier phase = (k / nst) mod 2, advanced
+    // per row (no division in the loop)
+    int s = 0;
+    uint32_t phase = 0;
     for (int64_t k = 0; k < nrows; ++k) {
-        const int s = (int)(k % nst);
-        const int64_t base = (blockIdx.x + k * G) * a.stride;
-        if (!mbar_wait_bounded(&full[s], (uint32_t)((k / nst) & 1), a.err)) gave_up = true;
+        const int64_t row = blockIdx.x + k * G;
+        const int64_t base = row * a.stride;
+        if constexpr (MODE == kAdalnShared) {
+            const uint32_t cr = (uint32_t)row / (uint32_t)a.rows_per_cond;   // the same in every thread
+            if (cr != c_cur) {
+                c_cur = cr;
+                const int64_t cbase = (int64_t)cr * a.cond_stride;
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                    const int c = threadIdx.x + i * blockDim.x;
+                    if (c < nvec) {
+                        f32x2 wt[PR], sc[PR];
+                        widen16<T>(load_w(i), wt);
+                        widen16<T>(ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC), sc);
+                        const f32x2 one2 = f2_make(1.0f, 1.0f);
+#pragma unroll
+                        for (int q = 0; q < PR; ++q) wv[i][q] = f2_mul(wt[q], f2_add(one2, sc[q]));
+                        shc[i] = ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC);
+                    }
+                }
+            }
+        }
+        if (!mbar_wait_bounded(&full[s], phase, a.err)) gave_up = true;
 
         // s = x (+ residual) in binary32, kept in registers for the scale step;
         // the post-add sum is written back as the next residual stream
@@ -102,7 +138,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                     for (int q = 0; q < PR; ++q) sv[i][q] = f2_add(sv[i][q], rv[q]);
                     st_global<T, VEC>(s_out + base + (int64_t)c * VEC, narrow16<T>(sv[i]));
                 }
-                if constexpr (ADALN) {   // out of the stage before the barrier frees it
+                if constexpr (STAGE_COND) {   // out of the stage before the barrier frees it
                     scp[i] = *reinterpret_cast<const P *>(stage(s, 1) + (size_t)c * 16);
                     shp[i] = *reinterpret_cast<const P *>(stage(s, 2) + (size_t)c * 16);
                 }
@@ -116,20 +152,27 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
             fence_proxy_async_smem();
-            issue(k + nst);
+            issue(k + nst, s);
         }
         const float rrms = rsqrtf(total / hf + a.eps);
-        if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[blockIdx.x + k * G] = rrms;
+        if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[row] = rrms;
         const f32x2 rr2 = f2_make(rrms, rrms);
-        // y = (s * rrms) * w, one rounding to the storage type
+        // y = (s * rrms) * w [AdaLN: * (1 + scale) + shift], one rounding to the storage type
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
             if (c < nvec) {
                 f32x2 yv[PR];
+                if constexpr (MODE == kAdalnShared) {   // (s * rrms) * (w * (1 + scale)) + shift
+                    f32x2 sh[PR];
+                    widen16<T>(shc[i], sh);
 #pragma unroll
-                for (int q = 0; q < PR; ++q) yv[q] = f2_mul(f2_mul(sv[i][q], rr2), wv[i][q]);
-                if constexpr (ADALN) {   // y * (1 + scale) + shift
+                    for (int q = 0; q < PR; ++q) yv[q] = f2_fma(f2_mul(sv[i][q], rr2), wv[i][q], sh[q]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) yv[q] = f2_mul(f2_mul(sv[i][q], rr2), wv[i][q]);
+                }
+                if constexpr (STAGE_COND) {   // y * (1 + scale) + shift
                     f32x2 sc[PR], sh[PR];
                     widen16<T>(scp[i], sc);
                     widen16<T>(shp[i], sh);
@@ -140,13 +183,17 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                 st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(yv));
             }
         }
+        if (++s == nst) {
+            s = 0;
+            phase ^= 1u;
+        }
     }
     // A copy whose wait gave up may still be landing in shared memory: give
     // every stage's last phase one more bounded wait before the CTA exits.
     if (gave_up && threadIdx.x == 0) {
-        for (int s = 0; s < nst && s < nrows; ++s) {
-            const int64_t uses = (nrows - 1 - s) / nst + 1;
-            mbar_wait_bounded(&full[s], (uint32_t)((uses - 1) & 1), nullptr);
+        for (int j = 0; j < nst && j < nrows; ++j) {
+            const int64_t uses = (nrows - 1 - j) / nst + 1;
+            mbar_wait_bounded(&full[j], (uint32_t)((uses - 1) & 1), nullptr);
         }
     }
 }
@@ -177,6 +224,7 @@ const void *kernel_mode(int mode, int nv) {
     case kPlain: return kernel_nv<T, kPlain>(nv);
     case kResid: return kernel_nv<T, kResid>(nv);
     case kAdaln: return kernel_nv<T, kAdaln>(nv);
+    case kAdalnShared: return kernel_nv<T, kAdalnShared>(nv);
     }
     return nullptr;
 }
@@ -205,6 +253,7 @@ cudaError_t launch_dt(const FwdArgs &a, int mode, const RingPlan &p, cudaStream_
     case kPlain: return launch_nv<T, kPlain>(a, p, st);
     case kResid: return launch_nv<T, kResid>(a, p, st);
     case kAdaln: return launch_nv<T, kAdaln>(a, p, st);
+    case kAdalnShared: return launch_nv<T, kAdalnShared>(a, p, st);
     }
     return cudaErrorInvalidValue;
 }

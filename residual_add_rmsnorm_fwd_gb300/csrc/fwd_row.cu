@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
         for (int u = 0; u < U; ++u) {
             const int64_t row = grp * U + u;
             const int64_t base = row * a.stride;
-            const int64_t cbase = ADALN ? (row / a.rows_per_cond) * a.cond_stride : 0;
+            const int64_t cbase = ADALN ? (int64_t)((uint32_t)row / (uint32_t)a.rows_per_cond) * a.cond_stride : 0;
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 const int c = threadIdx.x + i * blockDim.x;

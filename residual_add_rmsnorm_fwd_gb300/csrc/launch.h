@@ -57,6 +57,10 @@ cudaError_t launch_fwd_ring(const FwdArgs &a, int dtype, int mode, const RingPla
 // (plain and residual-fused only; a.r selects the fused form).
 cudaError_t launch_fwd_small(const FwdArgs &a, int dtype, bool vec, int sm_count, cudaStream_t st);
 
+// 16-byte aligned rows of 512 B to 2 KB, plain and AdaLN: a warp per row.
+bool fwd_warp_fits(int H, int dtype);
+cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, int mode, int sm_count, cudaStream_t st);
+
 // Row kept in registers between the sum of squares and the scale step.
 bool fwd_row_fits(int H, int dtype, bool vec);
 cudaError_t launch_fwd_row(const FwdArgs &a, int dtype, int mode, bool vec, int sm_count, cudaStream_t st);

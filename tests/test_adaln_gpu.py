@@ -1,8 +1,9 @@
 """GPU parity of rmsnorm_adaln_fwd against the fp64 oracle: every kernel path
-(register rows for H < 256 and up to the register budget, the bulk-copy ring
-for aligned rows of 8 KB and more, the chunked two-pass kernel above), per-
-token and broadcast conditioning rows, padded and misaligned layouts, in
-place, with guard bands around every buffer.
+(register rows for H < 256 and up to the register budget, a warp per aligned
+row of 512 B to 2 KB when conditioning rows are shared by 8 rows or more,
+the bulk-copy ring for aligned rows of 8 KB and more, the chunked two-pass
+kernel above), per-token and broadcast conditioning rows, padded and
+misaligned layouts, in place, with guard bands around every buffer.
 
 Tolerance: y = t + shift may cancel, so each element is compared against
 y_scale = |t| + |shift| from the oracle: fp32 within 1e-5 * y_scale; f16 and
@@ -66,7 +67,7 @@ def assert_ok(res):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("H", H_ADALN)
-@pytest.mark.parametrize("rows_per_cond", [1, 5])
+@pytest.mark.parametrize("rows_per_cond", [1, 5, 64])
 def test_adaln_paths(oracle, dtype, H, rows_per_cond):
     assert_ok(run_adaln(oracle, dtype, rows_for(H), H, rows_per_cond=rows_per_cond, seed=H + rows_per_cond))
 
@@ -92,7 +93,8 @@ def test_adaln_strides_and_misalignment(oracle, dtype, H, stride, cond_stride, o
 
 @pytest.mark.parametrize("dtype,H,M,rpc", [("bf16", 1152, 20001, 4096), ("bf16", 4096, 6001, 1000),
                                            ("f16", 3072, 9001, 1), ("f32", 4096, 3001, 3001),
-                                           ("bf16", 64, 50001, 7)])
+                                           ("bf16", 64, 50001, 7), ("bf16", 1024, 30001, 512),
+                                           ("f32", 512, 20001, 64), ("f16", 256, 70001, 9)])
 def test_adaln_grid_stride(oracle, dtype, H, M, rpc):
     """More rows than resident CTAs; conditioning rows shared by many rows,
     a ragged last sequence, and a single conditioning row for all rows."""

@@ -9,8 +9,11 @@ ref, dx_scale) where dx_scale is the size of the two terms whose difference
 forms dx; dweight within the same rtol times sum_i |dy * xhat| per column.
 
 Kernel paths (chosen by H, dtype and layout): the lane-group kernel for
-H < 256, the register-resident row kernel, the chunked two-pass kernel for
-large H; each in a 128-bit variant (16-byte aligned rows) and a scalar one.
+H < 256, a warp per aligned row of 512 B to 2 KB (plain forward), the
+register-resident row kernel, the bulk-copy ring for aligned rows of 8 KB
+and more, the chunked two-pass kernel for large H; the lane-group, row and
+chunked kernels each in a 128-bit variant (16-byte aligned rows) and a
+scalar one.
 """
 import numpy as np
 import pytest
@@ -85,7 +88,8 @@ def test_fwd_paths(oracle, dtype, H, residual, weight):
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("H,stride,offset", [
     (64, 72, 0), (64, 67, 0), (1000, 1003, 0), (4096, 4096, 1), (4096, 4160, 0), (6144, 6272, 0),
-    (2048, 2049, 1), (200, 200, 3), (16384, 16392, 0), (16384, 16385, 1)])
+    (2048, 2049, 1), (200, 200, 3), (16384, 16392, 0), (16384, 16385, 1), (512, 520, 0), (1024, 1032, 0),
+    (768, 776, 0)])
 def test_fwd_strides_and_misalignment(oracle, dtype, H, stride, offset):
     for residual in (False, True):
         res = run_fwd(oracle, dtype, rows_for(H, 200_000), H, stride=stride, residual=residual,
@@ -98,6 +102,13 @@ def test_fwd_strides_and_misalignment(oracle, dtype, H, stride, offset):
 def test_fwd_grid_stride(oracle, dtype, H, M):
     """More rows than resident CTAs/warps: every CTA handles several rows."""
     assert_fwd_ok(run_fwd(oracle, dtype, M, H, residual=True, seed=M))
+
+
+@pytest.mark.parametrize("dtype,H,M", [("bf16", 1024, 40001), ("f16", 512, 90001), ("f32", 256, 70001),
+                                       ("bf16", 4096, 20001), ("bf16", 8192, 6001), ("f32", 4096, 9001)])
+def test_fwd_plain_grid_stride(oracle, dtype, H, M):
+    """The plain forward over many rows per warp (512 B - 2 KB rows) or per ring CTA."""
+    assert_fwd_ok(run_fwd(oracle, dtype, M, H, residual=False, seed=M + 1))
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
