@@ -285,28 +285,42 @@ void finish_ring(RingPlan *p, int nv, int threads, int64_t row_bytes, int stream
 
 }  // namespace
 
-// Forward: rows of at least 8 KB.  Two 16-byte groups per thread (four above
-// 1024 groups).  Measured on GB300 at H = 4096-8192:
-//   - residual-fused (two input rows per slot): two stages, two CTAs per
-//     SM; deeper rings or more CTAs per SM put more rows in flight and lose
-//     DRAM efficiency;
-//   - one input row per slot (plain, and AdaLN with shared conditioning
-//     rows): up to four CTAs per SM, two stages (three above 12 KB rows):
-//     plain bf16 H = 4096, 4862 -> 6185 GB/s against two CTAs; H = 8192,
-//     5907 -> 6305 GB/s with the third stage.
-// Shorter rows run faster on the register and warp kernels.
+// Forward ring geometry, measured on GB300 (bf16 unless noted, about 100-270
+// MB per call).  Two 16-byte groups per thread (four above 1024 groups).
+//   - One input row per slot (plain, and AdaLN with shared conditioning
+//     rows), from 4 KB rows: 4-6 KB rows two stages and up to eight CTAs per
+//     SM (H = 2048: 5431 -> 5653 GB/s against the register kernel); 6-8 KB
+//     rows four stages, four CTAs (H = 3072: 5043 -> 6293 GB/s); longer rows
+//     four CTAs and two stages, three above 12 KB (H = 4096: 4862 -> 6185
+//     GB/s against two CTAs; H = 8192: 5907 -> 6305 GB/s with the third
+//     stage).
+//   - Two or three input rows per slot (residual-fused, AdaLN with per-token
+//     conditioning), from 8 KB rows: two stages, two CTAs per SM; deeper
+//     rings or more CTAs per SM put more rows in flight and lose DRAM
+//     efficiency, and below 8 KB the register kernel was as fast.
 bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
     const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
-    if (row_bytes % 16 != 0 || row_bytes < 8192) return false;
+    const int streams = mode == kAdaln ? 3 : (mode == kResid ? 2 : 1);   // x (+ residual | scale, shift)
+    const bool one_stream = streams == 1;
+    if (row_bytes % 16 != 0 || row_bytes < (one_stream ? 4096 : 8192)) return false;
     const int nvec = (int)(row_bytes / 16);
     const int nv = nvec <= 1024 ? 2 : 4;
     const int threads = round_up_to(ceil_div(nvec, nv), 32);
     if (threads > 512) return false;
-    const int streams = mode == kAdaln ? 3 : (mode == kResid ? 2 : 1);   // x (+ residual | scale, shift)
-    const bool plain = streams == 1;   // plain, or AdaLN reading shared conditioning rows through L1
-    const int stages = plain && row_bytes > 12288 ? 3 : 2;
+    int stages = 2, cps = 2;
+    if (one_stream) {
+        if (row_bytes < 6144) {
+            cps = 8;
+        } else if (row_bytes < 8192) {
+            stages = 4;
+            cps = 4;
+        } else {
+            stages = row_bytes > 12288 ? 3 : 2;
+            cps = 4;
+        }
+    }
     if (kRingHeaderBytes + (size_t)stages * streams * round_up_to((int)row_bytes, 128) > 200 * 1024) return false;
-    finish_ring(p, nv, threads, row_bytes, streams, stages, plain ? 4 : 2);
+    finish_ring(p, nv, threads, row_bytes, streams, stages, cps);
     return true;
 }
 

@@ -119,14 +119,15 @@ def test_adaln_broadcast_is_bitwise_repeated_rows(oracle, dtype, H):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("H", [2048, 4096, 32768])
+@pytest.mark.parametrize("H", [1024, 2048, 3072, 4096, 32768])
 def test_adaln_zero_conditioning_is_bitwise_rmsnorm(oracle, dtype, H):
     """scale = shift = 0: y * (1 + 0) + 0 = y exactly, so the result equals
-    rmsnorm_fwd's bit for bit where both calls take the same kernel family
-    (below H = 256 the plain forward reduces a row in a lane group instead)."""
+    rmsnorm_fwd's bit for bit.  One conditioning row serves every row, which
+    takes the same kernel family as the plain forward from H = 256 up (below
+    that the plain forward reduces a row in a lane group instead)."""
     M = rows_for(H)
-    z = wl.to_storage(np.zeros((M, H), np.float32), dtype)
-    a = run_adaln(oracle, dtype, M, H, sc_np=z, sh_np=z, seed=13)
+    z = wl.to_storage(np.zeros((1, H), np.float32), dtype)
+    a = run_adaln(oracle, dtype, M, H, rows_per_cond=M, sc_np=z, sh_np=z, seed=13)
     assert_ok(a)
     xd = wl.to_torch(a["x"], dtype).cuda()
     wd = wl.to_torch(a["w"], dtype).cuda()
