@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for RMSNorm forward, residual-fused forward and backward.
+"""fp64 CPU oracle for RMSNorm forward, residual-fused forward and backward,
+the AdaLN forward and the residual + LayerNorm forward.
 
 TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the benchmark's
 CPU-baseline leg may import this package.  The library's product path never
@@ -68,6 +69,7 @@ def _load():
             lib.orc_rmsnorm_bwd.argtypes = [i32, p, p, p, i64, i64, i64, d, p, p, p, p, p, i32]
             lib.orc_rmsnorm_bwd_residual.argtypes = [i32, p, p, p, p, i64, i64, i64, d, p, p, p, p, p, i32]
             lib.orc_rmsnorm_adaln_fwd.argtypes = [i32, p, p, p, p, i64, i64, i64, i64, i64, d, p, p, p, i32]
+            lib.orc_layernorm_fwd.argtypes = [i32, p, p, p, p, i64, i64, i64, d, p, p, p, p, p, i32]
             for f in (lib.orc_decode, lib.orc_encode, lib.orc_rmsnorm_fwd, lib.orc_rmsnorm_bwd,
                       lib.orc_rmsnorm_bwd_residual, lib.orc_rmsnorm_adaln_fwd):
                 f.restype = i32
@@ -238,3 +240,40 @@ def rmsnorm_adaln_fwd(x, w, scale, shift, eps: float, dtype: str, rows_per_cond:
     if rc:
         raise ValueError(f"orc_rmsnorm_adaln_fwd failed ({rc})")
     return {"y": y, "y_scale": y_scale, "rrms": rrms}
+
+
+def layernorm_fwd(x, w, b, eps: float, dtype: str, residual=None, nthreads: int | None = None):
+    """Residual + LayerNorm forward (textbook LayerNorm: biased variance, eps
+    inside the square root; the devpost "SpeedROCm" page, item 4).  x,
+    residual: (M, H) storage; w, b: (H,) storage or None.  Returns float64
+    ``y``, ``y_scale`` ((|s| + |mean|) * rstd * |w| + |b|), ``s`` (M, H) and
+    ``mean``, ``rstd`` (M,)."""
+    x, M, H, stride = _matrix(x, dtype, "x")
+    if residual is not None:
+        residual, Mr, Hr, sr = _matrix(residual, dtype, "residual")
+        if (Mr, Hr) != (M, H):
+            raise ValueError("residual shape differs from x")
+        if sr != stride:
+            x = np.ascontiguousarray(x)
+            residual = np.ascontiguousarray(residual)
+            stride = H
+    vecs = []
+    for v, name in ((w, "w"), (b, "b")):
+        if v is not None:
+            v = np.ascontiguousarray(v)
+            _check_storage(v, dtype, name)
+            if v.shape != (H,):
+                raise ValueError(f"{name} must have shape (H,)")
+        vecs.append(v)
+    w, b = vecs
+    y = np.empty((M, H), np.float64)
+    y_scale = np.empty((M, H), np.float64)
+    s = np.empty((M, H), np.float64)
+    mean = np.empty((M,), np.float64)
+    rstd = np.empty((M,), np.float64)
+    rc = _load().orc_layernorm_fwd(DTYPES[dtype], _ptr(x), _ptr(residual), _ptr(w), _ptr(b), M, H, stride,
+                                   eps_as_f32(eps), _ptr(y), _ptr(y_scale), _ptr(s), _ptr(mean), _ptr(rstd),
+                                   nthreads or default_threads())
+    if rc:
+        raise ValueError(f"orc_layernorm_fwd failed ({rc})")
+    return {"y": y, "y_scale": y_scale, "s": s, "mean": mean, "rstd": rstd}

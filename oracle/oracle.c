@@ -19,7 +19,8 @@
  *     of the fused forward (orc_rmsnorm_bwd_residual)
  * and the PyTorch one-liner printed on the "Rocm Kernels" page
  * (skillselion.com huggingface/kernels/rocm-kernels, "Compare with PyTorch
- * reference"), which states the same forward.
+ * reference"), which states the same forward.  It also holds that page's
+ * AdaLN forward and a residual + LayerNorm forward (see their sections).
  *
  * Everything is evaluated in IEEE binary64, in plain ascending index order,
  * with no blocking or reordering.  Storage formats are decoded to binary64 on
@@ -351,6 +352,83 @@ int orc_rmsnorm_adaln_fwd(int dtype, const void *x, const void *w, const void *s
     struct adaln_ctx c = {dtype, x, w, scale, shift, H, stride, cond_stride, rows_per_cond, eps, y, y_scale,
                           rrms};
     parallel_ranges(adaln_rows, &c, M, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Residual + LayerNorm forward (the devpost "SpeedROCm" page, How the      */
+/* solution addresses the problem, item 4: each residual add fused with the */
+/* LayerNorm that consumes it; the model's reference LayerNorm is PyTorch's,*/
+/* Development tools).  The pages print no formula; this is the textbook    */
+/* definition with the mean subtraction the RMSNorm skill page says         */
+/* LayerNorm has (Do not use this when, second bullet):                     */
+/*   s = x (+ r);  mean = sum(s) / H;  var = sum((s - mean)^2) / H          */
+/*   rstd = 1 / sqrt(var + eps);  y = (s - mean) * rstd * w + b             */
+/* (biased variance, eps inside the square root, per-column weight and      */
+/* bias), both sums in one pass each over the row, ascending.               */
+/* ------------------------------------------------------------------------ */
+
+struct ln_ctx {
+    int dtype;
+    const void *x, *r, *w, *b;
+    int64_t H, stride;
+    double eps;
+    double *y, *y_scale, *s_out, *mean, *rstd;
+};
+
+static void ln_rows(void *p, int64_t i0, int64_t i1)
+{
+    const struct ln_ctx *c = (const struct ln_ctx *)p;
+    const int64_t H = c->H;
+    double *s = (double *)malloc((size_t)H * sizeof(double));
+    if (!s)
+        abort();
+    for (int64_t i = i0; i < i1; ++i) {
+        const int64_t row = i * c->stride;
+        for (int64_t h = 0; h < H; ++h) {
+            s[h] = load_elem(c->dtype, c->x, row + h);
+            if (c->r)
+                s[h] += load_elem(c->dtype, c->r, row + h);
+        }
+        double sum = 0.0;
+        for (int64_t h = 0; h < H; ++h)
+            sum += s[h];
+        const double mean = sum / (double)H;
+        double sq = 0.0;
+        for (int64_t h = 0; h < H; ++h)
+            sq += (s[h] - mean) * (s[h] - mean);
+        const double rstd = 1.0 / sqrt(sq / (double)H + c->eps);
+        if (c->mean)
+            c->mean[i] = mean;
+        if (c->rstd)
+            c->rstd[i] = rstd;
+        for (int64_t h = 0; h < H; ++h) {
+            const double w = c->w ? load_elem(c->dtype, c->w, h) : 1.0;
+            const double b = c->b ? load_elem(c->dtype, c->b, h) : 0.0;
+            c->y[i * H + h] = ((s[h] - mean) * rstd) * w + b;
+            /* size of the terms whose differences and sum make y */
+            if (c->y_scale)
+                c->y_scale[i * H + h] = (fabs(s[h]) + fabs(mean)) * rstd * fabs(w) + fabs(b);
+            if (c->s_out)
+                c->s_out[i * H + h] = s[h];
+        }
+    }
+    free(s);
+}
+
+/*
+ * x, r (nullable), w (nullable: no weight), b (nullable: no bias) are storage
+ * arrays with the layout of orc_rmsnorm_fwd.  Outputs: y, y_scale, s_out
+ * (dense M x H), mean and rstd (M); all but y nullable.
+ */
+int orc_layernorm_fwd(int dtype, const void *x, const void *r, const void *w, const void *b,
+                      int64_t M, int64_t H, int64_t stride, double eps, double *y, double *y_scale,
+                      double *s_out, double *mean, double *rstd, int nthreads)
+{
+    if (!elem_size(dtype) || !x || !y || M < 0 || H <= 0 || stride < H)
+        return 1;
+    struct ln_ctx c = {dtype, x, r, w, b, H, stride, eps, y, y_scale, s_out, mean, rstd};
+    parallel_ranges(ln_rows, &c, M, nthreads);
     return 0;
 }
 

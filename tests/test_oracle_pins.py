@@ -356,3 +356,99 @@ def test_adaln_closed_form_single_column(oracle):
     want = x[:, 0] * 0.8 * (1 + sc[:, 0]) / np.sqrt(x[:, 0] ** 2 + e) + sh[:, 0]
     np.testing.assert_allclose(got["y"][:, 0], want, rtol=1e-15)
     assert np.all(got["y_scale"] >= np.abs(got["y"]))
+
+
+# ------------------------------------------------------- residual + LayerNorm --
+# The pages name the fused residual + LayerNorm ("SpeedROCm" page, item 4) but
+# print no formula; the oracle takes the textbook LayerNorm (biased variance,
+# eps inside the square root, per-column weight and bias).  These pins tie it
+# to PyTorch's own LayerNorm (an independent implementation), to closed forms
+# and to the RMSNorm oracle.
+
+def test_layernorm_matches_torch_layer_norm(oracle):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(50)
+    M, H = 7, 96
+    x = rng.standard_normal((M, H)) * 3 + 1.5
+    w = 1 + 0.1 * rng.standard_normal(H)
+    b = 0.2 * rng.standard_normal(H)
+    e = oracle.eps_as_f32(1e-5)
+    for wv, bv in ((w, b), (None, None), (w, None), (None, b)):
+        got = oracle.layernorm_fwd(x, wv, bv, 1e-5, "f64")
+        want = torch.nn.functional.layer_norm(
+            torch.from_numpy(x), (H,), None if wv is None else torch.from_numpy(wv),
+            None if bv is None else torch.from_numpy(bv), eps=e).numpy()
+        np.testing.assert_allclose(got["y"], want, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(got["mean"], x.mean(axis=1), rtol=1e-13)
+
+
+def test_layernorm_output_moments(oracle):
+    """w = 1, b = 0: every row of y has mean 0 and mean square var / (var + eps)."""
+    rng = np.random.default_rng(51)
+    x = rng.standard_normal((5, 64)) * np.array([[0.01], [1], [10], [100], [0.3]]) + 7
+    eps = 1e-3
+    out = oracle.layernorm_fwd(x, None, None, eps, "f64")
+    var = ((x - x.mean(axis=1, keepdims=True)) ** 2).mean(axis=1)
+    e = oracle.eps_as_f32(eps)
+    np.testing.assert_allclose(out["y"].mean(axis=1), 0, atol=1e-12)
+    np.testing.assert_allclose((out["y"] ** 2).mean(axis=1), var / (var + e), rtol=1e-12)
+    np.testing.assert_allclose(out["rstd"], 1 / np.sqrt(var + e), rtol=1e-12)
+
+
+def test_layernorm_shift_invariance(oracle):
+    """LayerNorm(x + c) = LayerNorm(x) for a constant c (integer data: the adds are exact)."""
+    rng = np.random.default_rng(52)
+    x = rng.integers(-50, 50, (4, 33)).astype(np.float64)
+    w = 1 + 0.1 * rng.standard_normal(33)
+    b = rng.standard_normal(33)
+    a = oracle.layernorm_fwd(x, w, b, 1e-5, "f64")["y"]
+    c = oracle.layernorm_fwd(x + 1000.0, w, b, 1e-5, "f64")["y"]
+    np.testing.assert_allclose(a, c, rtol=1e-13, atol=1e-13)
+
+
+def test_layernorm_constant_rows_give_the_bias(oracle):
+    """H = 1, or a constant row: s - mean = 0, so y = b exactly and rstd = 1/sqrt(eps)."""
+    b = np.array([0.75, -2.0, 0.5])
+    x = np.array([[4.0, 4.0, 4.0], [-1.5, -1.5, -1.5]])
+    out = oracle.layernorm_fwd(x, np.array([3.0, 2.0, 1.0]), b, 1e-4, "f64")
+    assert np.array_equal(out["y"], np.tile(b, (2, 1)))
+    np.testing.assert_allclose(out["rstd"], 1 / np.sqrt(oracle.eps_as_f32(1e-4)), rtol=1e-15)
+    assert np.array_equal(out["mean"], np.array([4.0, -1.5]))
+    one = oracle.layernorm_fwd(np.array([[2.5], [-7.0]]), np.array([5.0]), np.array([0.125]), 1e-5, "f64")
+    assert np.array_equal(one["y"][:, 0], np.array([0.125, 0.125]))
+
+
+def test_layernorm_two_columns_closed_form(oracle):
+    """s = [a, c]: mean = (a + c)/2, var = d^2 with d = (a - c)/2, y = (+-d / sqrt(d^2 + eps)) w + b."""
+    a, c, eps = 3.0, -1.0, 0.5
+    w, b = np.array([2.0, 0.5]), np.array([0.1, -0.3])
+    out = oracle.layernorm_fwd(np.array([[a, c]]), w, b, eps, "f64")
+    d = (a - c) / 2
+    e = oracle.eps_as_f32(eps)
+    want = np.array([d, -d]) / np.sqrt(d * d + e) * w + b
+    np.testing.assert_allclose(out["y"][0], want, rtol=1e-15)
+    assert out["mean"][0] == 1.0
+
+
+def test_layernorm_residual_fusion_equals_add_then_norm(oracle):
+    rng = np.random.default_rng(53)
+    x, r = rng.standard_normal((6, 40)), rng.standard_normal((6, 40))
+    w, b = 1 + 0.1 * rng.standard_normal(40), rng.standard_normal(40)
+    fused = oracle.layernorm_fwd(x, w, b, 1e-5, "f64", residual=r)
+    plain = oracle.layernorm_fwd(x + r, w, b, 1e-5, "f64")
+    assert np.array_equal(fused["y"], plain["y"])
+    assert np.array_equal(fused["s"], x + r)
+
+
+def test_layernorm_of_zero_mean_rows_is_rmsnorm(oracle):
+    """With a row mean of exactly 0 the variance is the mean square: LayerNorm without
+    bias equals the RMSNorm oracle on the same row."""
+    rng = np.random.default_rng(54)
+    v = rng.standard_normal((5, 16))
+    x = np.concatenate([v, -v], axis=1)        # exact zero mean
+    w = 1 + 0.1 * rng.standard_normal(32)
+    ln = oracle.layernorm_fwd(x, w, None, 1e-5, "f64")
+    rms = oracle.rmsnorm_fwd(x, w, 1e-5, "f64")
+    np.testing.assert_allclose(ln["y"], rms["y"], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(ln["rstd"], rms["rrms"], rtol=1e-14)
+    assert np.all(ln["y_scale"] >= np.abs(ln["y"]))
