@@ -133,6 +133,33 @@ int rmsnorm_adaln_fwd(const void *x, const void *weight, const void *scale, cons
                       int dtype, int has_weight, void *stream);
 
 /*
+ * Residual + LayerNorm forward.  (The devpost "SpeedROCm" page, How the
+ * solution addresses the problem, item 4: each residual add fused with the
+ * LayerNorm that consumes it.  The pages print no LayerNorm formula; this is
+ * the textbook one, with the mean subtraction the RMSNorm skill page
+ * contrasts RMSNorm with, Do not use this when, second bullet.)  Per row:
+ *   s = x (+ residual), binary32; residual_out = s rounded to dtype
+ *   mean = sum(s) / H;  var = sum((s - mean)^2) / H  (biased; the centred
+ *     sum comes from the row held on chip, or from a re-read of rows longer
+ *     than the register and shared-memory budget)
+ *   rstd = 1 / sqrt(var + eps);  y = ((s - mean) * rstd) * weight + bias
+ *   x, residual   in   M x H, row_stride (residual: fused form only)
+ *   weight, bias  in   H elements each; ignored (may be NULL) when
+ *                      has_weight / has_bias == 0 (weight 1, bias 0)
+ *   y             out  M x H, row_stride (may be x itself)
+ *   residual_out  out  M x H, row_stride (fused form; may be the residual)
+ *   mean, rstd    out  M binary32 values each, or NULL
+ * No backward is provided for these calls.
+ */
+int layernorm_fwd(const void *x, const void *weight, const void *bias, void *y,
+                  float *mean, float *rstd, int64_t row_stride, int64_t M, int64_t H,
+                  float eps, int dtype, int has_weight, int has_bias, void *stream);
+int layernorm_fwd_residual(const void *x, const void *residual, const void *weight,
+                           const void *bias, void *y, void *residual_out, float *mean,
+                           float *rstd, int64_t row_stride, int64_t M, int64_t H, float eps,
+                           int dtype, int has_weight, int has_bias, void *stream);
+
+/*
  * Size in bytes of the workspace rmsnorm_bwd (and rmsnorm_bwd_residual)
  * needs for (M, H, dtype) on the current device (per-CTA binary32 dweight
  * partials).  Writes *bytes; the

@@ -246,8 +246,9 @@ def layernorm_fwd(x, w, b, eps: float, dtype: str, residual=None, nthreads: int 
     """Residual + LayerNorm forward (textbook LayerNorm: biased variance, eps
     inside the square root; the devpost "SpeedROCm" page, item 4).  x,
     residual: (M, H) storage; w, b: (H,) storage or None.  Returns float64
-    ``y``, ``y_scale`` ((|s| + |mean|) * rstd * |w| + |b|), ``s`` (M, H) and
-    ``mean``, ``rstd`` (M,)."""
+    ``y``, ``y_scale`` ((|s| + mean(|s|)) * rstd * |w| + |b|: the size of the
+    terms y is formed from, mean(|s|) bounding the mean's rounding), ``s``
+    (M, H) and ``mean``, ``rstd`` (M,)."""
     x, M, H, stride = _matrix(x, dtype, "x")
     if residual is not None:
         residual, Mr, Hr, sr = _matrix(residual, dtype, "residual")

@@ -390,10 +390,13 @@ static void ln_rows(void *p, int64_t i0, int64_t i1)
             if (c->r)
                 s[h] += load_elem(c->dtype, c->r, row + h);
         }
-        double sum = 0.0;
-        for (int64_t h = 0; h < H; ++h)
+        double sum = 0.0, abs_sum = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
             sum += s[h];
+            abs_sum += fabs(s[h]);
+        }
         const double mean = sum / (double)H;
+        const double mean_abs = abs_sum / (double)H;   /* condition scale of the mean */
         double sq = 0.0;
         for (int64_t h = 0; h < H; ++h)
             sq += (s[h] - mean) * (s[h] - mean);
@@ -406,9 +409,11 @@ static void ln_rows(void *p, int64_t i0, int64_t i1)
             const double w = c->w ? load_elem(c->dtype, c->w, h) : 1.0;
             const double b = c->b ? load_elem(c->dtype, c->b, h) : 0.0;
             c->y[i * H + h] = ((s[h] - mean) * rstd) * w + b;
-            /* size of the terms whose differences and sum make y */
+            /* size of the terms whose differences and sum make y: s_h, the
+             * mean (whose rounding error in any evaluation scales with the
+             * mean of |s|) and the bias */
             if (c->y_scale)
-                c->y_scale[i * H + h] = (fabs(s[h]) + fabs(mean)) * rstd * fabs(w) + fabs(b);
+                c->y_scale[i * H + h] = (fabs(s[h]) + mean_abs) * rstd * fabs(w) + fabs(b);
             if (c->s_out)
                 c->s_out[i * H + h] = s[h];
         }

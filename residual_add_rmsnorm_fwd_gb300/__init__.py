@@ -22,7 +22,8 @@ import threading
 
 __all__ = [
     "RMSN_F32", "RMSN_F16", "RMSN_BF16", "RmsnormError", "lib", "lib_path",
-    "rmsnorm_fwd", "rmsnorm_fwd_residual", "rmsnorm_adaln_fwd", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
+    "rmsnorm_fwd", "rmsnorm_fwd_residual", "rmsnorm_adaln_fwd", "layernorm_fwd", "layernorm_fwd_residual",
+    "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
     "rmsnorm_bwd_residual", "rmsnorm_bwd_noalloc", "rmsnorm_read_device_errors", "rmsnorm_status_string",
     "dtype_code",
 ]
@@ -62,6 +63,8 @@ def lib():
             L.rmsnorm_fwd.argtypes = [p, p, p, p, i64, i64, i64, f32, i32, i32, p]
             L.rmsnorm_fwd_residual.argtypes = [p, p, p, p, p, p, i64, i64, i64, f32, i32, i32, p]
             L.rmsnorm_adaln_fwd.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64, f32, i32, i32, p]
+            L.layernorm_fwd.argtypes = [p, p, p, p, p, p, i64, i64, i64, f32, i32, i32, i32, p]
+            L.layernorm_fwd_residual.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64, f32, i32, i32, i32, p]
             L.rmsnorm_bwd_workspace_bytes.argtypes = [i64, i64, i32, ctypes.POINTER(sz)]
             L.rmsnorm_bwd.argtypes = [p, p, p, p, p, p, p, sz, i64, i64, i64, i32, i32, p]
             L.rmsnorm_bwd_residual.argtypes = [p, p, p, p, p, p, p, p, sz, i64, i64, i64, i32, i32, p]
@@ -158,6 +161,26 @@ def rmsnorm_adaln_fwd(x, weight, scale, shift, y, rows_per_cond: int = 1, rrms=N
     _check("rmsnorm_adaln_fwd", lib().rmsnorm_adaln_fwd(
         _ptr(x), _ptr(weight), _ptr(scale), _ptr(shift), _ptr(y), _ptr(rrms), stride, cond_stride,
         int(rows_per_cond), M, H, float(eps), dtype_code(x.dtype), int(weight is not None), _stream(stream)))
+
+
+def layernorm_fwd(x, weight, bias, y, mean=None, rstd=None, eps: float = 1e-5, stream=None):
+    """y = (x - mean(x)) * rsqrt(var(x) + eps) * weight + bias (biased
+    variance); ``weight`` / ``bias`` None means none; mean and rstd (M,) fp32
+    are saved when given."""
+    M, H, stride = _shared_stride([(x, "x"), (y, "y")])
+    _check("layernorm_fwd", lib().layernorm_fwd(
+        _ptr(x), _ptr(weight), _ptr(bias), _ptr(y), _ptr(mean), _ptr(rstd), stride, M, H, float(eps),
+        dtype_code(x.dtype), int(weight is not None), int(bias is not None), _stream(stream)))
+
+
+def layernorm_fwd_residual(x, residual, weight, bias, y, residual_out, mean=None, rstd=None, eps: float = 1e-5,
+                           stream=None):
+    """residual_out = x + residual; y = LayerNorm(x + residual) * weight + bias."""
+    M, H, stride = _shared_stride([(x, "x"), (residual, "residual"), (y, "y"), (residual_out, "residual_out")])
+    _check("layernorm_fwd_residual", lib().layernorm_fwd_residual(
+        _ptr(x), _ptr(residual), _ptr(weight), _ptr(bias), _ptr(y), _ptr(residual_out), _ptr(mean), _ptr(rstd),
+        stride, M, H, float(eps), dtype_code(x.dtype), int(weight is not None), int(bias is not None),
+        _stream(stream)))
 
 
 def rmsnorm_read_device_errors() -> int:

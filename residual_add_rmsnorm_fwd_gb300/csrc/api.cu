@@ -112,13 +112,14 @@ bool rows_vectorisable(int64_t H, int64_t stride, int dtype) {
 int to_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA; }
 
 // Kernel family by row length and layout: lane groups below 256 elements
-// (plain and residual-fused; AdaLN takes the register kernel there), a warp
+// (plain and residual-fused; AdaLN and LayerNorm take the register kernel
+// there), a warp
 // per aligned row of 512 B to 2 KB (plain, and AdaLN whose conditioning rows
 // are each shared by at least 8 rows), the bulk-copy ring for aligned rows
 // of at least 8 KB, the register kernel, and the two-pass chunked kernel
 // above the register budget.
 int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, int sms, cudaStream_t s) {
-    if (a.H < kSmallH && mode != kAdaln) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
+    if (a.H < kSmallH && (mode == kPlain || mode == kResid)) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
     const bool shared_cond = mode == kAdaln && a.rows_per_cond >= 8;
     if (vec && (mode == kPlain || shared_cond) && fwd_warp_fits(a.H, dtype))
         return to_status(launch_fwd_warp(a, dtype, mode, sms, s));
@@ -249,6 +250,72 @@ int adaln_forward(const void *x, const void *weight, const void *scale, const vo
     return dispatch_fwd(a, dtype, kAdaln, vec, sms, static_cast<cudaStream_t>(stream));
 }
 
+// Residual + LayerNorm forward: validation as for the RMSNorm forward, plus
+// the bias and the saved mean.
+int layernorm_forward(const void *x, const void *residual, const void *weight, const void *bias, void *y,
+                      void *residual_out, float *mean, float *rstd, int64_t row_stride, int64_t M, int64_t H,
+                      float eps, int dtype, int has_weight, int has_bias, void *stream, bool fused) {
+    int st = check_shape(M, H, row_stride, dtype);
+    if (st) return st;
+    if (!std::isfinite(eps) || eps < 0.0f) return RMSN_ERR_INVALID;
+    if ((has_weight && weight == nullptr) || (has_bias && bias == nullptr)) return RMSN_ERR_INVALID;
+    if (M > 0) {
+        if (x == nullptr || y == nullptr) return RMSN_ERR_INVALID;
+        if (fused && (residual == nullptr || residual_out == nullptr)) return RMSN_ERR_INVALID;
+    }
+    const int es = elem_bytes(dtype);
+    const void *w = has_weight ? weight : nullptr;
+    const void *b = has_bias ? bias : nullptr;
+    const void *r = fused ? residual : nullptr;
+    void *so = fused ? residual_out : nullptr;
+    for (const void *p : {x, r, w, b, static_cast<const void *>(y), static_cast<const void *>(so)})
+        if (p != nullptr && !aligned(p, es)) return RMSN_ERR_INVALID;
+    if ((rstd != nullptr && !aligned(rstd, 4)) || (mean != nullptr && !aligned(mean, 4))) return RMSN_ERR_INVALID;
+
+    const Range rx = matrix_of(x, M, H, row_stride, es);
+    const Range rr = matrix_of(r, M, H, row_stride, es);
+    const Range rw = bytes_of(w, (size_t)H * es);
+    const Range rb = bytes_of(b, (size_t)H * es);
+    const Range ry = matrix_of(y, M, H, row_stride, es);
+    const Range rs = matrix_of(so, M, H, row_stride, es);
+    const Range rq = bytes_of(rstd, (size_t)M * sizeof(float));
+    const Range rm = bytes_of(mean, (size_t)M * sizeof(float));
+    const Range outs[] = {ry, rs, rq, rm};
+    const Range all[] = {rx, rr, rw, rb, ry, rs, rq, rm};
+    // in place: y may be x itself and residual_out the residual itself
+    for (int o = 0; o < 4; ++o)
+        for (int k = 0; k < 8; ++k) {
+            const bool same = (o == 0 && k == 0 && y == x) || (o == 1 && k == 1 && so == r);
+            if (k != 4 + o && !same && overlap(outs[o], all[k])) return RMSN_ERR_ALIAS;
+        }
+
+    if (M == 0) return RMSN_OK;
+    int dev = 0, sms = 0;
+    st = current_device(&dev, &sms);
+    if (st) return st;
+
+    bool vec = rows_vectorisable(H, row_stride, dtype);
+    for (const void *p : {x, r, w, b, static_cast<const void *>(y), static_cast<const void *>(so)})
+        if (p != nullptr && !aligned(p, 16)) vec = false;
+
+    FwdArgs a{};
+    a.err = device_error_word(dev);
+    a.x = x;
+    a.r = r;
+    a.w = w;
+    a.b = b;
+    a.y = y;
+    a.s_out = so;
+    a.rrms = rstd;
+    a.mean = mean;
+    a.stride = row_stride;
+    a.M = M;
+    a.H = (int)H;
+    a.eps = eps;
+    a.has_w = has_weight ? 1 : 0;
+    return dispatch_fwd(a, dtype, fused ? kLnResid : kLn, vec, sms, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 cudaError_t allow_dynamic_smem(const void *func, size_t bytes) {
@@ -300,7 +367,8 @@ void finish_ring(RingPlan *p, int nv, int threads, int64_t row_bytes, int stream
 //     efficiency, and below 8 KB the register kernel was as fast.
 bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
     const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
-    const int streams = mode == kAdaln ? 3 : (mode == kResid ? 2 : 1);   // x (+ residual | scale, shift)
+    // x (+ residual | scale, shift)
+    const int streams = mode == kAdaln ? 3 : ((mode == kResid || mode == kLnResid) ? 2 : 1);
     const bool one_stream = streams == 1;
     if (row_bytes % 16 != 0 || row_bytes < (one_stream ? 4096 : 8192)) return false;
     const int nvec = (int)(row_bytes / 16);
@@ -461,6 +529,21 @@ RMSN_API int rmsnorm_adaln_fwd(const void *x, const void *weight, const void *sc
                                int64_t M, int64_t H, float eps, int dtype, int has_weight, void *stream) {
     return adaln_forward(x, weight, scale, shift, y, rrms, row_stride, cond_stride, rows_per_cond, M, H, eps, dtype,
                          has_weight, stream);
+}
+
+RMSN_API int layernorm_fwd(const void *x, const void *weight, const void *bias, void *y, float *mean, float *rstd,
+                           int64_t row_stride, int64_t M, int64_t H, float eps, int dtype, int has_weight,
+                           int has_bias, void *stream) {
+    return layernorm_forward(x, nullptr, weight, bias, y, nullptr, mean, rstd, row_stride, M, H, eps, dtype,
+                             has_weight, has_bias, stream, false);
+}
+
+RMSN_API int layernorm_fwd_residual(const void *x, const void *residual, const void *weight, const void *bias,
+                                    void *y, void *residual_out, float *mean, float *rstd, int64_t row_stride,
+                                    int64_t M, int64_t H, float eps, int dtype, int has_weight, int has_bias,
+                                    void *stream) {
+    return layernorm_forward(x, residual, weight, bias, y, residual_out, mean, rstd, row_stride, M, H, eps, dtype,
+                             has_weight, has_bias, stream, true);
 }
 
 RMSN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype, size_t *bytes) {

@@ -33,6 +33,10 @@ struct FwdArgs {
     const void *shift;
     int64_t cond_stride;
     int64_t rows_per_cond;   // 1..M (clamped to M by the host), so row / rows_per_cond fits 32 bits
+    // LayerNorm: bias (H,) or nullptr, and the saved per-row mean (M) or
+    // nullptr; rrms then holds the per-row rstd
+    const void *b;
+    float *mean;
 };
 
 // Forward variants: plain norm, residual-fused, AdaLN (norm * w * (1 + scale)
@@ -40,7 +44,9 @@ struct FwdArgs {
 // by many rows: the bulk-copy ring then reads them through L1 instead of
 // staging a copy per row (every SM copying the same few rows from L2 makes
 // those L2 lines a hot spot); the other kernels read them through L1 always.
-enum FwdMode { kPlain = 0, kResid = 1, kAdaln = 2, kAdalnShared = 3 };
+// kLn / kLnResid are LayerNorm, plain and residual-fused: ((s - mean) *
+// rstd) * w + b with the mean and the centred variance of the row.
+enum FwdMode { kPlain = 0, kResid = 1, kAdaln = 2, kAdalnShared = 3, kLn = 4, kLnResid = 5 };
 
 struct BwdArgs {
     const void *dy;

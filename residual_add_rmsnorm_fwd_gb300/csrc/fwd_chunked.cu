@@ -1,5 +1,6 @@
-// fwd_chunked.cu -- RMSNorm forward (plain, residual-fused, AdaLN) for
-// hidden sizes above the register budget of the row kernel.
+// fwd_chunked.cu -- RMSNorm forward (plain, residual-fused, AdaLN) and
+// residual + LayerNorm forward for hidden sizes above the register budget of
+// the row kernel.
 //
 // Two passes over each row with identical chunk bounds ("Skill: Write a
 // Triton RMSNorm Kernel", Required reasoning 11; Kernel design rules, last
@@ -7,21 +8,25 @@
 // pass 2 re-reads the chunks (the row was just read, so the re-read is
 // mostly served by L2), recomputes the identical binary32 s = x + residual,
 // and writes residual_out and y (AdaLN: y * (1 + scale) + shift, "Rocm
-// Kernels" page, 4. AdaLN).  One CTA per row, persistent grid.
+// Kernels" page, 4. AdaLN).  LayerNorm makes three passes: the sum (the
+// mean), the centred sum of squares, then the output.  One CTA per row,
+// persistent grid.
 #include "launch.h"
 
 namespace rmsn {
 
 template <typename T, int VEC, int MODE>
 __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
-    constexpr bool RESID = MODE == kResid;
+    constexpr bool RESID = MODE == kResid || MODE == kLnResid;
     constexpr bool ADALN = MODE == kAdaln;
+    constexpr bool LN = MODE == kLn || MODE == kLnResid;
     using P = Pack<T, VEC>;
     constexpr int U = 2;  // vectors per thread per chunk (independent loads in flight)
     __shared__ float red[64];
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
+    const T *__restrict__ bias = static_cast<const T *>(a.b);
     const T *__restrict__ scale = static_cast<const T *>(a.scale);
     const T *__restrict__ shift = static_cast<const T *>(a.shift);
     T *__restrict__ y = static_cast<T *>(a.y);
@@ -34,41 +39,67 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * a.stride;
         const int64_t cbase = ADALN ? (int64_t)((uint32_t)row / (uint32_t)a.rows_per_cond) * a.cond_stride : 0;
-        float ss = 0.0f;
-        for (int c0 = 0; c0 < nvec; c0 += chunk) {
-            P xp[U], rp[U];
+        // one pass over the row's chunks: accumulates sum(s^2), sum(s) or
+        // (LayerNorm's second pass) sum((s - centre)^2), s = x (+ residual)
+        auto reduce_pass = [&](int kind, float centre) {
+            float acc = 0.0f;
+            for (int c0 = 0; c0 < nvec; c0 += chunk) {
+                P xp[U], rp[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int c = c0 + u * blockDim.x + threadIdx.x;
-                if (c < nvec) {
-                    xp[u] = ld_cached<T, VEC>(x + base + (int64_t)c * VEC);
-                    if constexpr (RESID) rp[u] = ld_cached<T, VEC>(r + base + (int64_t)c * VEC);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int c = c0 + u * blockDim.x + threadIdx.x;
-                if (c < nvec) {
-                    float v[VEC];
-                    unpack(xp[u], v);
-                    if constexpr (RESID) {
-                        float rv[VEC];
-                        unpack(rp[u], rv);
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + u * blockDim.x + threadIdx.x;
+                    if (c < nvec) {
+                        xp[u] = ld_cached<T, VEC>(x + base + (int64_t)c * VEC);
+                        if constexpr (RESID) rp[u] = ld_cached<T, VEC>(r + base + (int64_t)c * VEC);
                     }
+                }
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) ss += v[j] * v[j];
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + u * blockDim.x + threadIdx.x;
+                    if (c < nvec) {
+                        float v[VEC];
+                        unpack(xp[u], v);
+                        if constexpr (RESID) {
+                            float rv[VEC];
+                            unpack(rp[u], rv);
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) v[j] += rv[j];
+                        }
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            if (kind == 1) {
+                                acc += v[j];
+                            } else {
+                                const float d = v[j] - centre;
+                                acc += d * d;
+                            }
+                        }
+                    }
                 }
             }
+            return acc;
+        };
+        float mu = 0.0f;
+        float total;
+        if constexpr (LN) {   // the mean, then the centred sum of squares (a second re-read)
+            total = block_sum(reduce_pass(1, 0.0f), red, bank);
+            bank ^= 1;
+            mu = total / hf;
+            total = block_sum(reduce_pass(0, mu), red, bank);
+            bank ^= 1;
+        } else {
+            total = block_sum(reduce_pass(0, 0.0f), red, bank);
+            bank ^= 1;
         }
-        const float total = block_sum(ss, red, bank);
-        bank ^= 1;
         const float rrms = rsqrtf(total / hf + a.eps);
-        if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[row] = rrms;
+        if (threadIdx.x == 0) {
+            if (a.rrms != nullptr) a.rrms[row] = rrms;
+            if constexpr (LN)
+                if (a.mean != nullptr) a.mean[row] = mu;
+        }
 
         for (int c0 = 0; c0 < nvec; c0 += chunk) {
-            P xp[U], rp[U], wp[U], scp[U], shp[U];
+            P xp[U], rp[U], wp[U], bp[U], scp[U], shp[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * blockDim.x + threadIdx.x;
@@ -76,6 +107,9 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
                     xp[u] = ld_stream<T, VEC>(x + base + (int64_t)c * VEC);
                     if constexpr (RESID) rp[u] = ld_stream<T, VEC>(r + base + (int64_t)c * VEC);
                     wp[u] = a.has_w ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+                    if constexpr (LN)
+                        bp[u] = bias != nullptr ? ld_cached<T, VEC>(bias + (int64_t)c * VEC)
+                                                : fill<T, VEC>(from_f32<T>(0.0f));
                     if constexpr (ADALN) {
                         scp[u] = ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC);
                         shp[u] = ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC);
@@ -96,8 +130,15 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
                         st_global<T, VEC>(s_out + base + (int64_t)c * VEC, pack<T, VEC>(v));
                     }
                     unpack(wp[u], wv);
+                    if constexpr (LN) {   // ((s - mean) * rstd) * w + b
+                        float bv[VEC];
+                        unpack(bp[u], bv);
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
+                        for (int j = 0; j < VEC; ++j) v[j] = fmaf((v[j] - mu) * rrms, wv[j], bv[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
+                    }
                     if constexpr (ADALN) {   // y * (1 + scale) + shift
                         float sc[VEC], sh[VEC];
                         unpack(scp[u], sc);
@@ -131,6 +172,8 @@ cudaError_t launch_mode(const FwdArgs &a, int mode, int sm_count, cudaStream_t s
     case kPlain: return launch_t<T, VEC, kPlain>(a, sm_count, st);
     case kResid: return launch_t<T, VEC, kResid>(a, sm_count, st);
     case kAdaln: return launch_t<T, VEC, kAdaln>(a, sm_count, st);
+    case kLn: return launch_t<T, VEC, kLn>(a, sm_count, st);
+    case kLnResid: return launch_t<T, VEC, kLnResid>(a, sm_count, st);
     }
     return cudaErrorInvalidValue;
 }

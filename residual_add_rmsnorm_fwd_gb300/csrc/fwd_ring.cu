@@ -18,8 +18,10 @@
 // rows (one per sequence) are read through L1 only when the CTA's row moves
 // to another one, and kept as w * (1 + scale) and shift in registers, so a
 // row costs one fused multiply-add per element more than the plain norm.
-// The stage is refilled with row k + NST as soon as the reduction barrier
-// shows every thread has copied it out.
+// LayerNorm (kLn, kLnResid) reduces the row twice from the same registers:
+// the sum for the mean, then the centred sum of squares; y = ((s - mean) *
+// rstd) * w + b.  The stage is refilled with row k + NST as soon as the
+// first reduction barrier shows every thread has copied it out.
 #include "bulk.cuh"
 #include "launch.h"
 
@@ -27,8 +29,9 @@ namespace rmsn {
 
 template <typename T, int NV, int MODE>
 __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) {
-    constexpr bool RESID = MODE == kResid;
+    constexpr bool RESID = MODE == kResid || MODE == kLnResid;
     constexpr bool ADALN = MODE == kAdaln || MODE == kAdalnShared;
+    constexpr bool LN = MODE == kLn || MODE == kLnResid;
     constexpr bool STAGE_COND = MODE == kAdaln;           // scale/shift rows staged beside x
     constexpr int VEC = Vec16<T>::n;
     constexpr int PR = Pairs16<T>::n;                     // binary32 pairs per 16-byte group
@@ -44,6 +47,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     const T *__restrict__ w = static_cast<const T *>(a.w);
     const T *__restrict__ scale = static_cast<const T *>(a.scale);
     const T *__restrict__ shift = static_cast<const T *>(a.shift);
+    const T *__restrict__ bias = static_cast<const T *>(a.b);
     T *__restrict__ y = static_cast<T *>(a.y);
     T *__restrict__ s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
@@ -89,6 +93,15 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     }
     P shc[NV];
     uint32_t c_cur = 0xffffffffu;
+    P bp[NV];   // LayerNorm bias, kept packed; zeros without one
+    if constexpr (LN) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = threadIdx.x + i * blockDim.x;
+            bp[i] = (bias != nullptr && c < nvec) ? ld_cached<T, VEC>(bias + (int64_t)c * VEC)
+                                                  : fill<T, VEC>(from_f32<T>(0.0f));
+        }
+    }
 
     int bank = 0;
     bool gave_up = false;
@@ -142,20 +155,48 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                     scp[i] = *reinterpret_cast<const P *>(stage(s, 1) + (size_t)c * 16);
                     shp[i] = *reinterpret_cast<const P *>(stage(s, 2) + (size_t)c * 16);
                 }
+                if constexpr (LN) {   // LayerNorm: the plain sum first (the mean)
 #pragma unroll
-                for (int q = 0; q < PR; ++q) ss2 = f2_fma(sv[i][q], sv[i][q], ss2);
+                    for (int q = 0; q < PR; ++q) ss2 = f2_add(ss2, sv[i][q]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) ss2 = f2_fma(sv[i][q], sv[i][q], ss2);
+                }
             }
         }
         // the barrier inside the reduction also means every thread has
         // copied stage s out, so it can be refilled
-        const float total = block_sum(f2_sum(ss2), red, bank);
+        float total = block_sum(f2_sum(ss2), red, bank);
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
             fence_proxy_async_smem();
             issue(k + nst, s);
         }
-        const float rrms = rsqrtf(total / hf + a.eps);
-        if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[row] = rrms;
+        float mu = 0.0f;
+        if constexpr (LN) {   // centre the row held in registers: s <- s - mean, then its sum of squares
+            mu = total / hf;
+            const f32x2 nm2 = f2_make(-mu, -mu);
+            ss2 = f2_make(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int c = threadIdx.x + i * blockDim.x;
+                if (c < nvec) {
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) {
+                        sv[i][q] = f2_add(sv[i][q], nm2);
+                        ss2 = f2_fma(sv[i][q], sv[i][q], ss2);
+                    }
+                }
+            }
+            total = block_sum(f2_sum(ss2), red, bank);
+            bank ^= 1;
+        }
+        const float rrms = rsqrtf(total / hf + a.eps);   // LayerNorm: rstd of the centred row
+        if (threadIdx.x == 0) {
+            if (a.rrms != nullptr) a.rrms[row] = rrms;
+            if constexpr (LN)
+                if (a.mean != nullptr) a.mean[row] = mu;
+        }
         const f32x2 rr2 = f2_make(rrms, rrms);
         // y = (s * rrms) * w [AdaLN: * (1 + scale) + shift], one rounding to the storage type
 #pragma unroll
@@ -168,6 +209,11 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                     widen16<T>(shc[i], sh);
 #pragma unroll
                     for (int q = 0; q < PR; ++q) yv[q] = f2_fma(f2_mul(sv[i][q], rr2), wv[i][q], sh[q]);
+                } else if constexpr (LN) {   // ((s - mean) * rstd) * w + b
+                    f32x2 bv[PR];
+                    widen16<T>(bp[i], bv);
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) yv[q] = f2_fma(f2_mul(sv[i][q], rr2), wv[i][q], bv[q]);
                 } else {
 #pragma unroll
                     for (int q = 0; q < PR; ++q) yv[q] = f2_mul(f2_mul(sv[i][q], rr2), wv[i][q]);
@@ -225,6 +271,8 @@ const void *kernel_mode(int mode, int nv) {
     case kResid: return kernel_nv<T, kResid>(nv);
     case kAdaln: return kernel_nv<T, kAdaln>(nv);
     case kAdalnShared: return kernel_nv<T, kAdalnShared>(nv);
+    case kLn: return kernel_nv<T, kLn>(nv);
+    case kLnResid: return kernel_nv<T, kLnResid>(nv);
     }
     return nullptr;
 }
@@ -254,6 +302,8 @@ cudaError_t launch_dt(const FwdArgs &a, int mode, const RingPlan &p, cudaStream_
     case kResid: return launch_nv<T, kResid>(a, p, st);
     case kAdaln: return launch_nv<T, kAdaln>(a, p, st);
     case kAdalnShared: return launch_nv<T, kAdalnShared>(a, p, st);
+    case kLn: return launch_nv<T, kLn>(a, p, st);
+    case kLnResid: return launch_nv<T, kLnResid>(a, p, st);
     }
     return cudaErrorInvalidValue;
 }

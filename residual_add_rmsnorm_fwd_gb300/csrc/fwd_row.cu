@@ -15,8 +15,9 @@ namespace rmsn {
 
 template <typename T, int VEC, int NV, int MODE, int U>
 __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
-    constexpr bool RESID = MODE == kResid;
+    constexpr bool RESID = MODE == kResid || MODE == kLnResid;
     constexpr bool ADALN = MODE == kAdaln;
+    constexpr bool LN = MODE == kLn || MODE == kLnResid;
     using P = Pack<T, VEC>;
     // 16-byte groups compute on binary32 pairs (two-lane f32x2 instructions);
     // the scalar path (unaligned rows) one element at a time
@@ -26,6 +27,7 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
     const T *__restrict__ x = static_cast<const T *>(a.x);
     const T *__restrict__ r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
+    const T *__restrict__ bias = static_cast<const T *>(a.b);
     const T *__restrict__ scale = static_cast<const T *>(a.scale);
     const T *__restrict__ shift = static_cast<const T *>(a.shift);
     T *__restrict__ y = static_cast<T *>(a.y);
@@ -33,14 +35,17 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;   // exact: H < 2^24
 
-    // weight (H,), indexed by column only; ones when the norm has no weight.
-    // Kept packed (and x, residual too): widening again in the scale step is
-    // cheaper than the registers binary32 copies would take from occupancy.
-    P wp[NV];
+    // weight (and LayerNorm bias) (H,), indexed by column only; ones (zeros)
+    // when absent.  Kept packed (and x, residual too): widening again in the
+    // scale step is cheaper than the registers binary32 copies would take
+    // from occupancy.
+    P wp[NV], bp[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int c = threadIdx.x + i * blockDim.x;
         wp[i] = (a.has_w && c < nvec) ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
+        if constexpr (LN)
+            bp[i] = (bias != nullptr && c < nvec) ? ld_cached<T, VEC>(bias + (int64_t)c * VEC) : fill<T, VEC>(T(0.0f));
     }
 
     // U consecutive rows per pass: all their loads are issued before any
@@ -67,7 +72,24 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
                 }
             }
         }
-        // binary32 sum of squares (residual added in binary32 first); the
+        // s = x (+ residual) in binary32, from the packed registers
+        auto s_pairs = [&](int u, int i, f32x2 (&sv)[PR]) {
+            if constexpr (PAIRS) {
+                widen16<T>(xp[u][i], sv);
+                if constexpr (RESID) {
+                    f32x2 rv[PR];
+                    widen16<T>(rp[u][i], rv);
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) sv[q] = f2_add(sv[q], rv[q]);
+                }
+            }
+        };
+        auto s_one = [&](int u, int i) {
+            float v = to_f32(xp[u][i].v[0]);
+            if constexpr (RESID) v += to_f32(rp[u][i].v[0]);
+            return v;
+        };
+        // binary32 sum of squares (RMSNorm) or sum (LayerNorm's mean); the
         // post-add sum is written back as the next residual stream
         float ss[U];
 #pragma unroll
@@ -90,15 +112,18 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
                             for (int q = 0; q < PR; ++q) sv[q] = f2_add(sv[q], rv[q]);
                             st_global<T, VEC>(s_out + base + (int64_t)c * VEC, narrow16<T>(sv));
                         }
+                        if constexpr (LN) {
 #pragma unroll
-                        for (int q = 0; q < PR; ++q) ss2 = f2_fma(sv[q], sv[q], ss2);
-                    } else {
-                        float v = to_f32(xp[u][i].v[0]);
-                        if constexpr (RESID) {
-                            v += to_f32(rp[u][i].v[0]);
-                            s_out[base + c] = from_f32<T>(v);
+                            for (int q = 0; q < PR; ++q) ss2 = f2_add(ss2, sv[q]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < PR; ++q) ss2 = f2_fma(sv[q], sv[q], ss2);
                         }
-                        ss[u] += v * v;
+                    } else {
+                        const float v = s_one(u, i);
+                        if constexpr (RESID) s_out[base + c] = from_f32<T>(v);
+                        if constexpr (LN) ss[u] += v;
+                        else ss[u] += v * v;
                     }
                 }
             }
@@ -106,16 +131,56 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
         }
         block_sum_n<U>(ss, red, bank);
         bank ^= 1;
+        // LayerNorm: the mean, then the centred sum of squares from the same
+        // registers (a second reduction, no second read of the row)
+        float mu[U];
+        if constexpr (LN) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t row = grp * U + u;
+                mu[u] = ss[u] / hf;
+                const f32x2 nm2 = f2_make(-mu[u], -mu[u]);
+                ss[u] = 0.0f;
+                f32x2 ss2 = f2_make(0.0f, 0.0f);
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                    const int c = threadIdx.x + i * blockDim.x;
+                    if (row < a.M && c < nvec) {
+                        if constexpr (PAIRS) {
+                            f32x2 sv[PR];
+                            s_pairs(u, i, sv);
+#pragma unroll
+                            for (int q = 0; q < PR; ++q) {
+                                const f32x2 d = f2_add(sv[q], nm2);
+                                ss2 = f2_fma(d, d, ss2);
+                            }
+                        } else {
+                            const float d = s_one(u, i) - mu[u];
+                            ss[u] += d * d;
+                        }
+                    }
+                }
+                if constexpr (PAIRS) ss[u] = f2_sum(ss2);
+            }
+            block_sum_n<U>(ss, red, bank);
+            bank ^= 1;
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t row = grp * U + u;
             if (row >= a.M) continue;
             const int64_t base = row * a.stride;
             // mean over the full row length, eps inside the square root
+            // (LayerNorm: rstd of the centred row; rrms holds it)
             const float rrms = rsqrtf(ss[u] / hf + a.eps);
-            if (a.rrms != nullptr && threadIdx.x == 0) a.rrms[row] = rrms;
+            if (threadIdx.x == 0) {
+                if (a.rrms != nullptr) a.rrms[row] = rrms;
+                if constexpr (LN)
+                    if (a.mean != nullptr) a.mean[row] = mu[u];
+            }
             const f32x2 rr2 = f2_make(rrms, rrms);
-            // y = (s * rrms) * w, one rounding to the storage type
+            // y = (s * rrms) * w [LayerNorm: ((s - mean) * rstd) * w + b], one
+            // rounding to the storage type
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 const int c = threadIdx.x + i * blockDim.x;
@@ -130,8 +195,17 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
                             for (int q = 0; q < PR; ++q) sv[q] = f2_add(sv[q], rv[q]);
                         }
                         widen16<T>(wp[i], wv);
+                        if constexpr (LN) {
+                            f32x2 bv[PR];
+                            widen16<T>(bp[i], bv);
+                            const f32x2 nm2 = f2_make(-mu[u], -mu[u]);
 #pragma unroll
-                        for (int q = 0; q < PR; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
+                            for (int q = 0; q < PR; ++q)
+                                sv[q] = f2_fma(f2_mul(f2_add(sv[q], nm2), rr2), wv[q], bv[q]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < PR; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
+                        }
                         if constexpr (ADALN) {   // y * (1 + scale) + shift
                             f32x2 sc[PR], sh[PR];
                             widen16<T>(scp[u][i], sc);
@@ -142,9 +216,12 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
                         }
                         st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(sv));
                     } else {
-                        float v = to_f32(xp[u][i].v[0]);
-                        if constexpr (RESID) v += to_f32(rp[u][i].v[0]);
-                        v = (v * rrms) * to_f32(wp[i].v[0]);
+                        float v = s_one(u, i);
+                        if constexpr (LN) {
+                            v = fmaf((v - mu[u]) * rrms, to_f32(wp[i].v[0]), to_f32(bp[i].v[0]));
+                        } else {
+                            v = (v * rrms) * to_f32(wp[i].v[0]);
+                        }
                         if constexpr (ADALN) v = fmaf(v, 1.0f + to_f32(scp[u][i].v[0]), to_f32(shp[u][i].v[0]));
                         y[base + c] = from_f32<T>(v);
                     }
@@ -241,6 +318,8 @@ cudaError_t launch_mode(const FwdArgs &a, int mode, int nv, int threads, int sm_
     case kPlain: return launch_nv<T, VEC, kPlain>(a, nv, threads, sm_count, st);
     case kResid: return launch_nv<T, VEC, kResid>(a, nv, threads, sm_count, st);
     case kAdaln: return launch_nv<T, VEC, kAdaln>(a, nv, threads, sm_count, st);
+    case kLn: return launch_nv<T, VEC, kLn>(a, nv, threads, sm_count, st);
+    case kLnResid: return launch_nv<T, VEC, kLnResid>(a, nv, threads, sm_count, st);
     }
     return cudaErrorInvalidValue;
 }

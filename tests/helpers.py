@@ -106,11 +106,12 @@ def bwd_rtol(dtype: str) -> float:
     return 1e-5 if dtype == "f32" else 2e-2
 
 
-def check_adaln_values(got_bits: np.ndarray, ref64: np.ndarray, y_scale: np.ndarray, dtype: str, oracle) -> dict:
-    """AdaLN tolerance per element.  y = t + shift can cancel, so the binary32
-    evaluation error is relative to y_scale = |t| + |shift|, not to |y|:
-    fp32 within 1e-5 * y_scale; f16/bf16 within 1 ulp of the oracle's value
-    rounded to the storage type, or within 1e-5 * y_scale of it."""
+def check_scaled_values(got_bits: np.ndarray, ref64: np.ndarray, y_scale: np.ndarray, dtype: str, oracle) -> dict:
+    """Tolerance per element for outputs formed by sums that can cancel
+    (AdaLN's + shift; LayerNorm's - mean and + bias): the binary32 evaluation
+    error is relative to y_scale, the oracle's size of the terms y is formed
+    from, not to |y|: fp32 within 1e-5 * y_scale; f16/bf16 within 1 ulp of the
+    oracle's value rounded to the storage type, or within 1e-5 * y_scale."""
     got = oracle.decode(got_bits, dtype)
     err = np.abs(got - ref64)
     ok = err <= 1e-5 * y_scale

@@ -196,3 +196,50 @@ def test_adaln_conditioning_extent(lib):
     assert adaln(lib, rpc=2, y=SC + 2 * 64 * 2 - 2) == ALIAS
     assert adaln(lib, sc=None, sh=None, x=None, y=None, M=0) == OK
     assert adaln(lib, w=None, has_w=0, M=0) == OK
+
+
+B, MN = 0x900000, 0xa00000
+
+
+def ln(lib, fused=False, **kw):
+    a = dict(x=X, r=R, w=W, b=B, y=Y, s=S, mean=MN, rstd=Q, stride=64, M=4, H=64, eps=1e-5, dtype=2, has_w=1,
+             has_b=1)
+    a.update(kw)
+    if fused:
+        return lib.layernorm_fwd_residual(a["x"], a["r"], a["w"], a["b"], a["y"], a["s"], a["mean"], a["rstd"],
+                                          a["stride"], a["M"], a["H"], a["eps"], a["dtype"], a["has_w"],
+                                          a["has_b"], None)
+    return lib.layernorm_fwd(a["x"], a["w"], a["b"], a["y"], a["mean"], a["rstd"], a["stride"], a["M"], a["H"],
+                             a["eps"], a["dtype"], a["has_w"], a["has_b"], None)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("kw", [
+    dict(x=None), dict(y=None), dict(w=None), dict(b=None), dict(b=B + 1), dict(mean=MN + 2), dict(rstd=Q + 1),
+    dict(eps=-1.0), dict(eps=float("nan")), dict(stride=63), dict(dtype=7), dict(H=0),
+])
+def test_layernorm_invalid(lib, fused, kw):
+    assert ln(lib, fused, **kw) == INVALID
+
+
+@pytest.mark.parametrize("kw", [dict(r=None), dict(s=None), dict(r=R + 1)])
+def test_layernorm_residual_invalid(lib, kw):
+    assert ln(lib, True, **kw) == INVALID
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("kw", [
+    dict(y=B), dict(mean=Y + 8), dict(rstd=MN), dict(mean=X + 4), dict(y=W + 2), dict(rstd=B + 64),
+])
+def test_layernorm_alias(lib, fused, kw):
+    assert ln(lib, fused, **kw) == ALIAS
+
+
+def test_layernorm_optional_arguments(lib):
+    passed = lambda st: st not in (INVALID, ALIAS)   # validation passed; no GPU here to run it
+    assert passed(ln(lib, w=None, has_w=0, b=None, has_b=0))
+    assert passed(ln(lib, mean=None, rstd=None))
+    assert passed(ln(lib, y=X))                                    # in place
+    assert passed(ln(lib, True, y=X, s=R))                         # both in place
+    assert ln(lib, True, s=X) == ALIAS                             # residual_out over x is not in place
+    assert ln(lib, M=0, x=None, y=None) == OK

@@ -15,7 +15,7 @@ import pytest
 
 import residual_add_rmsnorm_fwd_gb300 as rn
 import workloads as wl
-from helpers import Guarded, check_adaln_values, device_vec, f32_buffer
+from helpers import Guarded, check_scaled_values, device_vec, f32_buffer
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -48,7 +48,7 @@ def run_adaln(oracle, dtype, M, H, rows_per_cond=1, stride=None, cond_stride=Non
     rn.rmsnorm_adaln_fwd(gx.t, wd, gsc.t, gsh.t, gy.t, rows_per_cond=rows_per_cond, rrms=rrms, eps=eps)
     torch.cuda.synchronize()
     ref = oracle.rmsnorm_adaln_fwd(x[:, :H], w, sc[:, :H], sh[:, :H], eps, dtype, rows_per_cond=rows_per_cond)
-    res = {"y": check_adaln_values(gy.host(), ref["y"], ref["y_scale"], dtype, oracle)}
+    res = {"y": check_scaled_values(gy.host(), ref["y"], ref["y_scale"], dtype, oracle)}
     got = rrms.cpu().numpy().astype(np.float64)
     res["rrms_bad"] = int(np.sum(~(np.abs(got - ref["rrms"]) <= 1e-5 * ref["rrms"])))
     assert gy.untouched_outside() and gsc.untouched_outside() and gsh.untouched_outside()
