@@ -208,12 +208,11 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
 
 // dweight_h = sum_{b = 0}^{G-1} partial[b][h].  A CTA covers 32 columns with
 // kReduceSlices warps; warp k sums the contiguous slice of partial rows
-// [k*G/S, (k+1)*G/S) in ascending order (eight loads in flight at a time,
+// [k*G/S, (k+1)*G/S) in ascending order (up to kReduceBatch loads in flight,
 // added one after another), then the slice sums are added in ascending k.
-// The order depends only on G, so the result is reproducible.  Launched as a
-// programmatic dependent of the backward kernel: its CTAs may start early
-// and wait here for that grid's completion and memory flush.
+// The order depends only on G, so the result is reproducible.
 constexpr int kReduceSlices = 32;
+constexpr int kReduceBatch = 24;
 
 __global__ void __launch_bounds__(32 * kReduceSlices)
     dweight_reduce_kernel(const float *__restrict__ partial, int G, int H, float *__restrict__ dweight) {
@@ -223,12 +222,16 @@ __global__ void __launch_bounds__(32 * kReduceSlices)
     float s = 0.0f;
     if (h < H) {
         const int g0 = (int)((int64_t)G * k / kReduceSlices), g1 = (int)((int64_t)G * (k + 1) / kReduceSlices);
-        for (int g = g0; g < g1; g += 8) {
-            float v[8];
+        // up to kReduceBatch loads in flight per thread: a slice of the
+        // usual 304-608 partial rows is one round trip to L2 (summed in
+        // ascending row order either way)
+        for (int g = g0; g < g1; g += kReduceBatch) {
+            float v[kReduceBatch];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = g + u < g1 ? __ldg(partial + (int64_t)(g + u) * H + h) : 0.0f;
+            for (int u = 0; u < kReduceBatch; ++u)
+                v[u] = g + u < g1 ? __ldg(partial + (int64_t)(g + u) * H + h) : 0.0f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) s += v[u];
+            for (int u = 0; u < kReduceBatch; ++u) s += v[u];
         }
     }
     part[k][col] = s;
