@@ -405,7 +405,7 @@ bool bwd_ring_geometry(int H, int dtype, bool dres, RingPlan *p) {
     const int nv = (dtype != kF16 && nvec <= 768) ? 2 : 4;
     const int threads = round_up_to(ceil_div(nvec, nv), 32);
     if (threads > 512) return false;
-    const int stages = 2;
+    const int stages = kBwdRingStages;
     const int streams = dres ? 3 : 2;
     const size_t smem = kRingHeaderBytes + (size_t)stages * streams * round_up_to((int)row_bytes, 128);
     if (smem > 200 * 1024) return false;

@@ -21,7 +21,11 @@
 namespace rmsn {
 
 template <typename T, int NV, bool DRES>
-__global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) {
+// The two-group DRES variants (at most 384 threads) are held to 80
+// registers: three CTAs of 256 threads per SM without spills measured
+// fastest; the other variants measured fastest with ptxas's own choice.
+__global__ void __launch_bounds__((NV == 2 && DRES) ? 384 : 512, (NV == 2 && DRES) ? 2 : 0)
+    bwd_ring_kernel(BwdArgs a, RingShape rs) {
     constexpr int VEC = Vec16<T>::n;
     constexpr int PR = Pairs16<T>::n;
     constexpr int NS = DRES ? 3 : 2;   // streams staged per row: dy, x (and dres)
@@ -38,7 +42,7 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
     T *__restrict__ dx = static_cast<T *>(a.dx);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
-    const int nst = rs.stages;
+    constexpr int nst = kBwdRingStages;   // rs.stages is the same value
     const int64_t G = gridDim.x;
     const int64_t nrows = (a.M - 1 - blockIdx.x) / G + 1;  // the grid never exceeds M
 
@@ -73,9 +77,8 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
     bool gave_up = false;
     float rr_next = __ldg(a.rrms + blockIdx.x);
     for (int64_t k = 0; k < nrows; ++k) {
-        // stage s = k mod nst and its mbarrier phase (k / nst) mod 2, in 32
-        // bits (rows per CTA < 2^31); a stage counter advanced per row, as in
-        // the forward ring, measured slower here (ptxas spilled)
+        // stage s = k mod nst and its mbarrier phase (k / nst) mod 2 (nst is
+        // a power-of-two constant: a mask and a shift)
         const int s = (int)((uint32_t)k % (uint32_t)nst);
         const uint32_t phase = ((uint32_t)k / (uint32_t)nst) & 1u;
         const int64_t base = (blockIdx.x + k * G) * a.stride;
@@ -112,6 +115,12 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
             fence_proxy_async_smem();
             issue(k + nst, s);
         }
+        // dx = rrms * (g - xhat * c).  With DRES it is evaluated as
+        // g * rrms + (x * (-rrms^2 c) + dres), the residual stream's gradient
+        // riding in the addend (measured faster there); without, as
+        // rrms * (g + xhat * (-c)) (measured faster there).
+        const float kx = -(rr * rr) * c_row;
+        const f32x2 kx2 = f2_make(kx, kx);
         const f32x2 nc2 = f2_make(-c_row, -c_row);
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
@@ -121,14 +130,15 @@ __global__ void __launch_bounds__(512) bwd_ring_kernel(BwdArgs a, RingShape rs) 
                 widen16<T>(gp[i], d);
                 widen16<T>(xp[i], xv);
                 widen16<T>(wp[i], wv);
-#pragma unroll
-                for (int q = 0; q < PR; ++q)   // rrms * (g - xhat * c)
-                    d[q] = f2_mul(rr2, f2_fma(f2_mul(xv[q], rr2), nc2, f2_mul(d[q], wv[q])));
-                if constexpr (DRES) {           // the residual stream's gradient joins ds
+                if constexpr (DRES) {
                     f32x2 rv[PR];
                     widen16<T>(rp[i], rv);
 #pragma unroll
-                    for (int q = 0; q < PR; ++q) d[q] = f2_add(d[q], rv[q]);
+                    for (int q = 0; q < PR; ++q) d[q] = f2_fma(f2_mul(d[q], wv[q]), rr2, f2_fma(xv[q], kx2, rv[q]));
+                } else {
+#pragma unroll
+                    for (int q = 0; q < PR; ++q)
+                        d[q] = f2_mul(rr2, f2_fma(f2_mul(xv[q], rr2), nc2, f2_mul(d[q], wv[q])));
                 }
                 st_global<T, VEC>(dx + base + (int64_t)c * VEC, narrow16<T>(d));
             }

@@ -74,6 +74,10 @@ struct RingShape {
 // its mbarriers (one 8-byte barrier per stage, at most 16 stages).
 constexpr int kRingHeaderBytes = 128;
 constexpr int kRingMaxStages = 16;
+// The backward ring always has two stages (measured best; the kernel takes the
+// count as a constant, so the stage index and mbarrier phase of row k are
+// bit operations).
+constexpr int kBwdRingStages = 2;
 
 // ---------------------------------------------------------------------------
 // Storage types
