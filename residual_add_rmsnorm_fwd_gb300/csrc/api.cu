@@ -352,40 +352,45 @@ void finish_ring(RingPlan *p, int nv, int threads, int64_t row_bytes, int stream
 
 }  // namespace
 
-// Forward ring geometry, measured on GB300 (bf16 unless noted, about 100-270
-// MB per call).  Two 16-byte groups per thread (four above 1024 groups).
-//   - One input row per slot (plain, and AdaLN with shared conditioning
-//     rows), from 4 KB rows: 4-6 KB rows two stages and up to eight CTAs per
-//     SM (H = 2048: 5431 -> 5653 GB/s against the register kernel); 6-8 KB
-//     rows four stages, four CTAs (H = 3072: 5043 -> 6293 GB/s); longer rows
-//     four CTAs and two stages, three above 12 KB (H = 4096: 4862 -> 6185
-//     GB/s against two CTAs; H = 8192: 5907 -> 6305 GB/s with the third
-//     stage).
-//   - Two or three input rows per slot (residual-fused, AdaLN with per-token
-//     conditioning), from 8 KB rows: two stages, two CTAs per SM; deeper
-//     rings or more CTAs per SM put more rows in flight and lose DRAM
-//     efficiency, and below 8 KB the register kernel was as fast.
+// Forward ring geometry, measured on GB300 (bf16 unless noted, 100-540 MB
+// per call).  Two 16-byte groups per thread (four above 1024 groups).  The
+// rule behind the table: about 64 KB of rows in flight per SM (stages x CTAs
+// per SM x input rows per slot x row bytes) -- less leaves HBM idle, more
+// loses DRAM efficiency -- with more CTAs per SM for short rows, whose fixed
+// per-row cost (wait, barrier, reduction, rsqrt) is paid by every thread.
+//   - One input row per slot (plain, LayerNorm, AdaLN with shared
+//     conditioning rows), from 4 KB rows: 4-6 KB 2 stages x 8 CTAs (H = 2048:
+//     5431 -> 5653 GB/s against the register kernel); 6-8 KB 4 x 4 (H = 3072:
+//     5043 -> 6293 GB/s); 8-16 KB 2 x 4 (H = 4096: 4862 -> 6185 GB/s against
+//     2 x 2; fp16 H = 6144: 6226 against 6106 at 2 x 3); from 16 KB 2 x 2
+//     (H = 8192: 5826 -> 6515 GB/s against 3 x 4; fp32 H = 4096: 5493 -> 6592).
+//   - Two input rows per slot (residual-fused, LayerNorm fused), from 8 KB
+//     rows: 8-12 KB 2 x 2 (deeper or wider measured slower); 12-16 KB 3 x 1
+//     (fp16 H = 6144: 5914 -> 6580 GB/s against 2 x 2); from 16 KB 2 x 1
+//     (H = 8192: 5941 -> 6319 GB/s; fp32 H = 4096: 5930 -> 6309 GB/s).
+//   - Three input rows per slot (AdaLN with per-token conditioning), from
+//     8 KB rows: 8-12 KB 2 x 3 (6510 -> 6742 GB/s against 2 x 2); longer 2 x 1.
+// Below these lengths the register and warp kernels were as fast or faster.
 bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
     const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
     // x (+ residual | scale, shift)
     const int streams = mode == kAdaln ? 3 : ((mode == kResid || mode == kLnResid) ? 2 : 1);
-    const bool one_stream = streams == 1;
-    if (row_bytes % 16 != 0 || row_bytes < (one_stream ? 4096 : 8192)) return false;
+    if (row_bytes % 16 != 0 || row_bytes < (streams == 1 ? 4096 : 8192)) return false;
     const int nvec = (int)(row_bytes / 16);
     const int nv = nvec <= 1024 ? 2 : 4;
     const int threads = round_up_to(ceil_div(nvec, nv), 32);
     if (threads > 512) return false;
+    constexpr int64_t KB = 1024;
     int stages = 2, cps = 2;
-    if (one_stream) {
-        if (row_bytes < 6144) {
-            cps = 8;
-        } else if (row_bytes < 8192) {
-            stages = 4;
-            cps = 4;
-        } else {
-            stages = row_bytes > 12288 ? 3 : 2;
-            cps = 4;
-        }
+    if (streams == 1) {
+        if (row_bytes < 6 * KB) cps = 8;
+        else if (row_bytes < 8 * KB) stages = 4, cps = 4;
+        else if (row_bytes < 16 * KB) cps = 4;
+    } else if (streams == 2) {
+        if (row_bytes >= 16 * KB) cps = 1;
+        else if (row_bytes >= 12 * KB) stages = 3, cps = 1;
+    } else {
+        cps = row_bytes < 12 * KB ? 3 : 1;
     }
     if (kRingHeaderBytes + (size_t)stages * streams * round_up_to((int)row_bytes, 128) > 200 * 1024) return false;
     finish_ring(p, nv, threads, row_bytes, streams, stages, cps);
