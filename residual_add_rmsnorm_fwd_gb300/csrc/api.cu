@@ -368,6 +368,8 @@ void finish_ring(RingPlan *p, int nv, int threads, int64_t row_bytes, int stream
 //     rows: 8-12 KB 2 x 2 (deeper or wider measured slower); 12-16 KB 3 x 1
 //     (fp16 H = 6144: 5914 -> 6580 GB/s against 2 x 2); from 16 KB 2 x 1
 //     (H = 8192: 5941 -> 6319 GB/s; fp32 H = 4096: 5930 -> 6309 GB/s).
+//     Fused LayerNorm at 8-12 KB: 1 x 4 (6146 -> 6310 GB/s; its second
+//     reduction per row favours more CTAs with one row each in flight).
 //   - Three input rows per slot (AdaLN with per-token conditioning), from
 //     8 KB rows: 8-12 KB 2 x 3 (6510 -> 6742 GB/s against 2 x 2); longer 2 x 1.
 // Below these lengths the register and warp kernels were as fast or faster.
@@ -389,6 +391,7 @@ bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
     } else if (streams == 2) {
         if (row_bytes >= 16 * KB) cps = 1;
         else if (row_bytes >= 12 * KB) stages = 3, cps = 1;
+        else if (mode == kLnResid) stages = 1, cps = 4;   // two reductions per row: more CTAs, one row each
     } else {
         cps = row_bytes < 12 * KB ? 3 : 1;
     }
