@@ -395,6 +395,7 @@ bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
     } else {
         cps = row_bytes < 12 * KB ? 3 : 1;
     }
+    if (stages > kRingMaxStages) return false;   // one mbarrier per stage in the ring header
     if (kRingHeaderBytes + (size_t)stages * streams * round_up_to((int)row_bytes, 128) > 200 * 1024) return false;
     finish_ring(p, nv, threads, row_bytes, streams, stages, cps);
     return true;
