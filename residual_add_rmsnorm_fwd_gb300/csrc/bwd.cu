@@ -118,9 +118,13 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
 }
 
 // H above the register budget: two passes over each row with identical chunk
-// bounds.  The CTA's dweight partial row lives in the workspace; it belongs
-// to this CTA alone, so it is updated with plain read-modify-write (the
-// first row of the CTA initialises it).
+// bounds.  The CTA's dweight partial row belongs to this CTA alone, each
+// column to one thread: it is accumulated in shared memory when H binary32
+// values fit (use_smem_acc; written to the workspace once at the end), else
+// updated in the workspace with 16-byte read-modify-writes (the first row of
+// the CTA initialises it).  Measured on GB300 at bf16 H = 32768: 1275 GB/s
+// with per-element updates in global memory, 2455 with 16-byte ones, 3062
+// in shared memory.
 template <typename T, int VEC, bool DRES>
 __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
     using P = Pack<T, VEC>;
@@ -135,6 +139,12 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
     const float hf = (float)a.H;
     const int chunk = blockDim.x * U;
     float *prow = a.partial != nullptr ? a.partial + (int64_t)blockIdx.x * a.H : nullptr;
+    extern __shared__ __align__(16) float sacc[];   // the CTA's partial row (H floats) when given
+    const bool use_s = prow != nullptr && (VEC % 4 == 0) && a.use_smem_acc;
+    if (use_s)
+        for (int c = threadIdx.x; c < nvec; c += blockDim.x)   // each thread's own columns
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) sacc[c * VEC + j] = 0.0f;
 
     int bank = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
@@ -189,21 +199,48 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
                     unpack(xp[u], xv);
                     unpack(wp[u], wv);
                     if constexpr (DRES) unpack(rp[u], rv);
+                    float pk[VEC];   // this row's dweight terms dy * xhat
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
                         const float xh = xv[j] * rr;
                         o[j] = rr * (d[j] * wv[j] - xh * c_row);
                         if constexpr (DRES) o[j] += rv[j];
-                        if (prow != nullptr) {
-                            float *p = prow + (int64_t)c * VEC + j;
-                            *p = first ? d[j] * xh : *p + d[j] * xh;
-                        }
+                        pk[j] = d[j] * xh;
                     }
                     st_global<T, VEC>(dx + base + (int64_t)c * VEC, pack<T, VEC>(o));
+                    if (use_s) {
+                        if constexpr (VEC % 4 == 0) {
+#pragma unroll
+                            for (int j = 0; j < VEC; j += 4) {
+                                float4 *q = reinterpret_cast<float4 *>(sacc + c * VEC + j);
+                                const float4 t = *q;
+                                *q = make_float4(t.x + pk[j], t.y + pk[j + 1], t.z + pk[j + 2], t.w + pk[j + 3]);
+                            }
+                        }
+                    } else if (prow != nullptr) {   // 16-byte read-modify-write of the CTA's own partial row
+                        float *p = prow + (int64_t)c * VEC;
+                        if constexpr (VEC % 4 == 0) {
+#pragma unroll
+                            for (int j = 0; j < VEC; j += 4) {
+                                float4 *q = reinterpret_cast<float4 *>(p + j);
+                                const float4 t = first ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : *q;
+                                *q = make_float4(t.x + pk[j], t.y + pk[j + 1], t.z + pk[j + 2], t.w + pk[j + 3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) p[j] = first ? pk[j] : p[j] + pk[j];
+                        }
+                    }
                 }
             }
         }
     }
+    if (use_s)   // the partial, built in shared memory, written once
+        for (int c = threadIdx.x; c < nvec; c += blockDim.x)
+#pragma unroll
+            for (int j = 0; j < VEC; j += 4)
+                *reinterpret_cast<float4 *>(prow + (int64_t)c * VEC + j) =
+                    *reinterpret_cast<const float4 *>(sacc + c * VEC + j);
 }
 
 // dweight_h = sum_{b = 0}^{G-1} partial[b][h].  A CTA covers 32 columns with
@@ -247,6 +284,7 @@ __global__ void __launch_bounds__(32 * kReduceSlices)
 namespace {
 
 constexpr int kRowMaxThreads = 512;
+constexpr size_t kChunkedSmemAccBytes = 160 * 1024;   // largest shared partial row of the chunked backward
 constexpr int kChunkThreads = 512;
 constexpr int kVecNV[] = {1, 2};
 constexpr int kScalarNV[] = {1, 2, 4, 8};
@@ -336,8 +374,10 @@ BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool dres, int sm_count)
     }
     const void *k = kernel_for(p, dtype, vec);
     int occ = 0;
-    if (k != nullptr && allow_dynamic_smem(k, p.smem_bytes) == cudaSuccess)
-        occ = occupancy(k, p.threads, p.smem_bytes);
+    size_t smem_occ = p.smem_bytes;   // the chunked kernel's shared partial row counts toward occupancy
+    if (p.kind == kBwdChunked && vec && (size_t)H * 4 <= kChunkedSmemAccBytes) smem_occ = (size_t)H * 4;
+    if (k != nullptr && allow_dynamic_smem(k, smem_occ) == cudaSuccess)
+        occ = occupancy(k, p.threads, smem_occ);
     const int64_t cap = (int64_t)(occ > 0 ? occ : 1) * sm_count;
     p.grid = (int)(M < cap ? (M > 0 ? M : 1) : cap);
     return p;
@@ -353,8 +393,15 @@ cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, 
     if (e != cudaSuccess) return e;
     BwdArgs args = a;
     RingShape shape = p.ring;
+    size_t smem = p.smem_bytes;
+    if (p.kind == kBwdChunked && vec && a.partial != nullptr && (size_t)a.H * 4 <= kChunkedSmemAccBytes) {
+        smem = (size_t)a.H * 4;
+        args.use_smem_acc = 1;
+        e = allow_dynamic_smem(k, smem);
+        if (e != cudaSuccess) return e;
+    }
     void *params[] = {&args, &shape};
-    e = cudaLaunchKernel(k, dim3((unsigned)p.grid), dim3((unsigned)p.threads), params, p.smem_bytes, st);
+    e = cudaLaunchKernel(k, dim3((unsigned)p.grid), dim3((unsigned)p.threads), params, smem, st);
     if (e != cudaSuccess) return e;
     if (dweight != nullptr && a.partial != nullptr) {
         e = launch_kernel(dweight_reduce_kernel, (unsigned)((a.H + 31) / 32), 32 * kReduceSlices, 0, st,

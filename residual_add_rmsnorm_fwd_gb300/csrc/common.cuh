@@ -61,6 +61,7 @@ struct BwdArgs {
     int H;
     int has_w;
     unsigned *err;
+    int use_smem_acc;     // chunked kernel: partial row accumulated in shared memory
 };
 
 // Geometry of a shared-memory row ring (bulk-copy kernels).
