@@ -113,20 +113,25 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA
 
 // Kernel family by row length and layout: lane groups below 256 elements
 // (plain and residual-fused; AdaLN and LayerNorm take the register kernel
-// there), a warp
-// per aligned row of 512 B to 2 KB (plain, and AdaLN whose conditioning rows
-// are each shared by at least 8 rows), the bulk-copy ring for aligned rows
-// of at least 8 KB, the register kernel, and the two-pass chunked kernel
-// above the register budget.
+// there), a warp per aligned row of 512 B to 2 KB (plain, and AdaLN whose
+// conditioning rows each serve 1024 rows or more), the bulk-copy ring for
+// aligned rows of 4 KB (one input stream) or 8 KB and more, the register
+// kernel, and the two-pass chunked kernel above the register budget.
 int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, int sms, cudaStream_t s) {
     if (a.H < kSmallH && (mode == kPlain || mode == kResid)) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
-    const bool shared_cond = mode == kAdaln && a.rows_per_cond >= 8;
-    if (vec && (mode == kPlain || shared_cond) && fwd_warp_fits(a.H, dtype))
+    // AdaLN conditioning rows count as shared when each serves at least four
+    // of a CTA's strides of rows, so a CTA rarely moves to a new one (below
+    // that, staging them beside x, or the register kernel, measured 10-45%
+    // faster: bf16 H = 4096 with 1024 rows per conditioning row, 4428 against
+    // 4954 GB/s), or when one conditioning row serves every row
+    if (vec && (mode == kPlain || (mode == kAdaln && a.rows_per_cond >= 1024)) && fwd_warp_fits(a.H, dtype))
         return to_status(launch_fwd_warp(a, dtype, mode, sms, s));
     RingPlan ring;
-    const int ring_mode = shared_cond ? kAdalnShared : mode;
-    if (vec && plan_fwd_ring(a.M, a.H, dtype, ring_mode, sms, &ring))
-        return to_status(launch_fwd_ring(a, dtype, ring_mode, ring, s));
+    if (vec && mode == kAdaln && plan_fwd_ring(a.M, a.H, dtype, kAdalnShared, sms, &ring) &&
+        (a.rows_per_cond >= 4 * (int64_t)ring.grid || a.rows_per_cond >= a.M))
+        return to_status(launch_fwd_ring(a, dtype, kAdalnShared, ring, s));
+    if (vec && plan_fwd_ring(a.M, a.H, dtype, mode, sms, &ring))
+        return to_status(launch_fwd_ring(a, dtype, mode, ring, s));
     if (fwd_row_fits(a.H, dtype, vec)) return to_status(launch_fwd_row(a, dtype, mode, vec, sms, s));
     return to_status(launch_fwd_chunked(a, dtype, mode, vec, sms, s));
 }

@@ -40,10 +40,11 @@ struct FwdArgs {
 };
 
 // Forward variants: plain norm, residual-fused, AdaLN (norm * w * (1 + scale)
-// + shift).  kAdalnShared is AdaLN whose conditioning rows are each shared
-// by many rows: the bulk-copy ring then reads them through L1 instead of
-// staging a copy per row (every SM copying the same few rows from L2 makes
-// those L2 lines a hot spot); the other kernels read them through L1 always.
+// + shift).  kAdalnShared is AdaLN whose conditioning rows each serve at
+// least four of a CTA's strides of rows (one row per sequence): the bulk-copy
+// ring then reads a conditioning row through L1 when the CTA's rows enter
+// it and keeps w * (1 + scale) and shift in registers, instead of staging
+// it beside every x row; the other kernels read conditioning through L1.
 // kLn / kLnResid are LayerNorm, plain and residual-fused: ((s - mean) *
 // rstd) * w + b with the mean and the centred variance of the row.
 enum FwdMode { kPlain = 0, kResid = 1, kAdaln = 2, kAdalnShared = 3, kLn = 4, kLnResid = 5 };

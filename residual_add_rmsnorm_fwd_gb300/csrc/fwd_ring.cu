@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
         for (int i = 0; i < NV; ++i) widen16<T>(load_w(i), wv[i]);
     }
     P shc[NV];
-    uint32_t c_cur = 0xffffffffu;
+    int64_t c_next = 0;   // first row of the next conditioning row: refresh when reached
     P bp[NV];   // LayerNorm bias, kept packed; zeros without one
     if constexpr (LN) {
 #pragma unroll
@@ -113,9 +113,11 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
         const int64_t row = blockIdx.x + k * G;
         const int64_t base = row * a.stride;
         if constexpr (MODE == kAdalnShared) {
-            const uint32_t cr = (uint32_t)row / (uint32_t)a.rows_per_cond;   // the same in every thread
-            if (cr != c_cur) {
-                c_cur = cr;
+            // rows of a CTA only increase: divide only when a boundary is passed
+            // (the same in every thread)
+            if (row >= c_next) {
+                const uint32_t cr = (uint32_t)row / (uint32_t)a.rows_per_cond;
+                c_next = (int64_t)(cr + 1) * a.rows_per_cond;
                 const int64_t cbase = (int64_t)cr * a.cond_stride;
 #pragma unroll
                 for (int i = 0; i < NV; ++i) {

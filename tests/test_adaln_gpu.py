@@ -1,9 +1,11 @@
 """GPU parity of rmsnorm_adaln_fwd against the fp64 oracle: every kernel path
 (register rows for H < 256 and up to the register budget, a warp per aligned
-row of 512 B to 2 KB when conditioning rows are shared by 8 rows or more,
-the bulk-copy ring for aligned rows of 8 KB and more, the chunked two-pass
-kernel above), per-token and broadcast conditioning rows, padded and
-misaligned layouts, in place, with guard bands around every buffer.
+row of 512 B to 2 KB when conditioning rows serve 1024 rows or more, the
+bulk-copy ring for aligned rows -- conditioning staged beside x, or held in
+registers when each conditioning row spans four of a CTA's row strides -- and the
+chunked two-pass kernel above), per-token and broadcast conditioning rows,
+padded and misaligned layouts, in place, with guard bands around every
+buffer.
 
 Tolerance: y = t + shift may cancel, so each element is compared against
 y_scale = |t| + |shift| from the oracle: fp32 within 1e-5 * y_scale; f16 and
@@ -94,7 +96,9 @@ def test_adaln_strides_and_misalignment(oracle, dtype, H, stride, cond_stride, o
 @pytest.mark.parametrize("dtype,H,M,rpc", [("bf16", 1152, 20001, 4096), ("bf16", 4096, 6001, 1000),
                                            ("f16", 3072, 9001, 1), ("f32", 4096, 3001, 3001),
                                            ("bf16", 64, 50001, 7), ("bf16", 1024, 30001, 512),
-                                           ("f32", 512, 20001, 64), ("f16", 256, 70001, 9)])
+                                           ("f32", 512, 20001, 64), ("f16", 256, 70001, 9),
+                                           ("bf16", 1024, 30001, 2048), ("f16", 512, 40001, 4096),
+                                           ("bf16", 2048, 20001, 5000)])
 def test_adaln_grid_stride(oracle, dtype, H, M, rpc):
     """More rows than resident CTAs; conditioning rows shared by many rows,
     a ragged last sequence, and a single conditioning row for all rows."""
@@ -124,8 +128,9 @@ def test_adaln_zero_conditioning_is_bitwise_rmsnorm(oracle, dtype, H):
     """scale = shift = 0: y * (1 + 0) + 0 = y exactly, so the result equals
     rmsnorm_fwd's bit for bit.  One conditioning row serves every row, which
     takes the same kernel family as the plain forward from H = 256 up (below
-    that the plain forward reduces a row in a lane group instead)."""
-    M = rows_for(H)
+    that the plain forward reduces a row in a lane group instead; a warp per
+    row needs conditioning rows serving 1024 rows, hence M >= 1025)."""
+    M = max(rows_for(H), 1025)
     z = wl.to_storage(np.zeros((1, H), np.float32), dtype)
     a = run_adaln(oracle, dtype, M, H, rows_per_cond=M, sc_np=z, sh_np=z, seed=13)
     assert_ok(a)
