@@ -1,6 +1,7 @@
-// fwd_ring.cu -- RMSNorm forward (plain, residual-fused, AdaLN) with rows
-// staged in shared memory by bulk copies (TMA), for 16-byte aligned rows of
-// LLM hidden sizes.
+// fwd_ring.cu -- RMSNorm forward (plain, residual-fused, AdaLN) and
+// LayerNorm forward with rows staged in shared memory by bulk copies (TMA),
+// for 16-byte aligned rows of LLM hidden sizes (from 4 KB with one input
+// stream, 8 KB with two or three).
 //
 // Persistent grid: CTA b owns rows b, b + G, b + 2G, ...  A ring of NST
 // shared-memory stages, each holding one row of x (and of the residual, or

@@ -1,5 +1,8 @@
-// fwd_row.cu -- RMSNorm forward (plain and residual-fused) for hidden sizes
-// whose row fits in the registers of one CTA.
+// fwd_row.cu -- RMSNorm forward (plain, residual-fused, AdaLN) and
+// LayerNorm forward for hidden sizes whose row fits in the registers of one
+// CTA: the general path for rows the warp and ring kernels do not take
+// (unaligned layouts, AdaLN and LayerNorm below H = 256, fused rows of 2-8
+// KB).
 //
 // One CTA per row, persistent: the grid holds as many CTAs as fit on the
 // device and each CTA strides over rows.  A thread owns NV fixed column
@@ -241,7 +244,7 @@ inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
 // Column groups per thread: the smallest CTA of at most 128, else 256, else
 // 512 threads that covers the row (measured: 128 threads x 2 groups is best
-// at H = 2048 bf16; larger aligned rows go to the bulk-copy ring kernel).
+// at H = 2048 bf16).
 bool pick(int nvec, bool vec, int &threads, int &nv) {
     const int *set = vec ? kVecNV : kScalarNV;
     const int n = vec ? 4 : 5;
