@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
     T *__restrict__ dx = static_cast<T *>(a.dx);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
+    const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
 
     P wp[NV];
     float acc[NV][VEC];
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
                 }
             }
         }
-        const float c_row = block_sum(dot, red, bank) / hf;
+        const float c_row = block_sum(dot, red, bank) * ih;
         bank ^= 1;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
     T *__restrict__ dx = static_cast<T *>(a.dx);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
+    const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
     const int chunk = blockDim.x * U;
     float *prow = a.partial != nullptr ? a.partial + (int64_t)blockIdx.x * a.H : nullptr;
     extern __shared__ __align__(16) float sacc[];   // the CTA's partial row (H floats) when given
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
                 }
             }
         }
-        const float c_row = block_sum(dot, red, bank) / hf;
+        const float c_row = block_sum(dot, red, bank) * ih;
         bank ^= 1;
         for (int c0 = 0; c0 < nvec; c0 += chunk) {
             P gp[U], xp[U], wp[U], rp[U];

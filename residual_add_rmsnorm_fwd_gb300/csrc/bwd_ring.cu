@@ -42,6 +42,7 @@ __global__ void __launch_bounds__((NV == 2 && DRES) ? 384 : 512, (NV == 2 && DRE
     T *__restrict__ dx = static_cast<T *>(a.dx);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
+    const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
     constexpr int nst = kBwdRingStages;   // rs.stages is the same value
     const int64_t G = gridDim.x;
     const int64_t nrows = (a.M - 1 - blockIdx.x) / G + 1;  // the grid never exceeds M
@@ -109,7 +110,7 @@ __global__ void __launch_bounds__((NV == 2 && DRES) ? 384 : 512, (NV == 2 && DRE
             }
         }
         // the reduction barrier also frees stage s for the row nst ahead
-        const float c_row = block_sum(f2_sum(dot2), red, bank) / hf;
+        const float c_row = block_sum(f2_sum(dot2), red, bank) * ih;
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
             fence_proxy_async_smem();

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
     T *__restrict__ s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
+    const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
     const int chunk = blockDim.x * U;
 
     int bank = 0;
@@ -84,14 +85,14 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
         if constexpr (LN) {   // the mean, then the centred sum of squares (a second re-read)
             total = block_sum(reduce_pass(1, 0.0f), red, bank);
             bank ^= 1;
-            mu = total / hf;
+            mu = total * ih;
             total = block_sum(reduce_pass(0, mu), red, bank);
             bank ^= 1;
         } else {
             total = block_sum(reduce_pass(0, 0.0f), red, bank);
             bank ^= 1;
         }
-        const float rrms = rsqrtf(total / hf + a.eps);
+        const float rrms = rsqrtf(total * ih + a.eps);
         if (threadIdx.x == 0) {
             if (a.rrms != nullptr) a.rrms[row] = rrms;
             if constexpr (LN)

@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     T *__restrict__ s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
+    const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
     const int nst = rs.stages;
     const int64_t G = gridDim.x;
     const int64_t nrows = (a.M - 1 - blockIdx.x) / G + 1;  // the grid never exceeds M
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
         }
         float mu = 0.0f;
         if constexpr (LN) {   // centre the row held in registers: s <- s - mean, then its sum of squares
-            mu = total / hf;
+            mu = total * ih;
             const f32x2 nm2 = f2_make(-mu, -mu);
             ss2 = f2_make(0.0f, 0.0f);
 #pragma unroll
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
             total = block_sum(f2_sum(ss2), red, bank);
             bank ^= 1;
         }
-        const float rrms = rsqrtf(total / hf + a.eps);   // LayerNorm: rstd of the centred row
+        const float rrms = rsqrtf(total * ih + a.eps);   // LayerNorm: rstd of the centred row
         if (threadIdx.x == 0) {
             if (a.rrms != nullptr) a.rrms[row] = rrms;
             if constexpr (LN)

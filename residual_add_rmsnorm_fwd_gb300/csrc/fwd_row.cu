@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
     T *__restrict__ s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;   // exact: H < 2^24
+    const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
 
     // weight (and LayerNorm bias) (H,), indexed by column only; ones (zeros)
     // when absent.  Kept packed (and x, residual too): widening again in the
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t row = grp * U + u;
-                mu[u] = ss[u] / hf;
+                mu[u] = ss[u] * ih;
                 const f32x2 nm2 = f2_make(-mu[u], -mu[u]);
                 ss[u] = 0.0f;
                 f32x2 ss2 = f2_make(0.0f, 0.0f);
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
             const int64_t base = row * a.stride;
             // mean over the full row length, eps inside the square root
             // (LayerNorm: rstd of the centred row; rrms holds it)
-            const float rrms = rsqrtf(ss[u] / hf + a.eps);
+            const float rrms = rsqrtf(ss[u] * ih + a.eps);
             if (threadIdx.x == 0) {
                 if (a.rrms != nullptr) a.rrms[row] = rrms;
                 if constexpr (LN)

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(256) fwd_small_kernel(FwdArgs a) {
     T *__restrict__ s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
+    const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
     const int lane = threadIdx.x & 31;
     const int slot = lane / LANES;   // which of the warp's rows
     const int li = lane % LANES;     // lane within the row's group
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(256) fwd_small_kernel(FwdArgs a) {
             }
             if constexpr (VEC > 1) ss = f2_sum(ss2);
             const float total = group_sum<LANES>(ss);
-            const float rrms = rsqrtf(total / hf + a.eps);
+            const float rrms = rsqrtf(total * ih + a.eps);
             if (live && li == 0 && a.rrms != nullptr) a.rrms[row] = rrms;
             const f32x2 rr2 = f2_make(rrms, rrms);
 #pragma unroll

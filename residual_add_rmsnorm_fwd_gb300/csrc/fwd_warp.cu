@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(256) fwd_warp_kernel(FwdArgs a) {
     T *__restrict__ s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
+    const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(256) fwd_warp_kernel(FwdArgs a) {
                 }
             }
             const float total = group_sum<32>(f2_sum(ss2));
-            const float rrms = rsqrtf(total / hf + a.eps);
+            const float rrms = rsqrtf(total * ih + a.eps);
             if (lane == 0 && a.rrms != nullptr) a.rrms[row] = rrms;
             const f32x2 rr2 = f2_make(rrms, rrms);
             // row / rows_per_cond in 32 bits: both are below 2^31
