@@ -7,8 +7,8 @@
 // rule): pass 1 accumulates the binary32 sum of squares chunk by chunk;
 // pass 2 re-reads the chunks (the row was just read, so the re-read is
 // mostly served by L2), recomputes the identical binary32 s = x + residual,
-// and writes residual_out and y (AdaLN: y * (1 + scale) + shift, "Rocm
-// Kernels" page, 4. AdaLN).  LayerNorm makes three passes: the sum (the
+// and writes residual_out and y (AdaLN: (s * rrms) * (w * (1 + scale)) +
+// shift, "Rocm Kernels" page, 4. AdaLN).  LayerNorm makes three passes: the sum (the
 // mean), the centred sum of squares, then the output.  One CTA per row,
 // persistent grid.
 #include "launch.h"
@@ -136,16 +136,15 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
                         unpack(bp[u], bv);
 #pragma unroll
                         for (int j = 0; j < VEC; ++j) v[j] = fmaf((v[j] - mu) * rrms, wv[j], bv[j]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
-                    }
-                    if constexpr (ADALN) {   // y * (1 + scale) + shift
+                    } else if constexpr (ADALN) {   // (s * rrms) * (w * (1 + scale)) + shift
                         float sc[VEC], sh[VEC];
                         unpack(scp[u], sc);
                         unpack(shp[u], sh);
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) v[j] = fmaf(v[j], 1.0f + sc[j], sh[j]);
+                        for (int j = 0; j < VEC; ++j) v[j] = fmaf(v[j] * rrms, wv[j] * (1.0f + sc[j]), sh[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];
                     }
                     st_global<T, VEC>(y + base + (int64_t)c * VEC, pack<T, VEC>(v));
                 }

@@ -14,7 +14,9 @@
 // sum(s^2) over the CTA, and writes y = (s * rrms) * w from registers: the
 // row is read from HBM once ("Skill: Write a Triton RMSNorm Kernel",
 // Required reasoning 3-10; Performance requirements).  AdaLN ("Rocm
-// Kernels" page, 4. AdaLN) continues y * (1 + scale) + shift: per-token
+// Kernels" page, 4. AdaLN) is evaluated as (s * rrms) * (w * (1 + scale)) +
+// shift, the last multiply and add fused, in every kernel, so conditioning
+// shared by rows gives the bits of the same rows repeated: per-token
 // conditioning rows are staged beside x; conditioning rows shared by many
 // rows (one per sequence) are read through L1 only when the CTA's row moves
 // to another one, and kept as w * (1 + scale) and shift in registers, so a
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                 if (a.mean != nullptr) a.mean[row] = mu;
         }
         const f32x2 rr2 = f2_make(rrms, rrms);
-        // y = (s * rrms) * w [AdaLN: * (1 + scale) + shift], one rounding to the storage type
+        // y = (s * rrms) * w [AdaLN: (s * rrms) * (w * (1 + scale)) + shift], one rounding to the storage type
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int c = threadIdx.x + i * blockDim.x;
@@ -218,17 +220,17 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                     widen16<T>(bp[i], bv);
 #pragma unroll
                     for (int q = 0; q < PR; ++q) yv[q] = f2_fma(f2_mul(sv[i][q], rr2), wv[i][q], bv[q]);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < PR; ++q) yv[q] = f2_mul(f2_mul(sv[i][q], rr2), wv[i][q]);
-                }
-                if constexpr (STAGE_COND) {   // y * (1 + scale) + shift
+                } else if constexpr (STAGE_COND) {   // (s * rrms) * (w * (1 + scale)) + shift
                     f32x2 sc[PR], sh[PR];
                     widen16<T>(scp[i], sc);
                     widen16<T>(shp[i], sh);
                     const f32x2 one2 = f2_make(1.0f, 1.0f);
 #pragma unroll
-                    for (int q = 0; q < PR; ++q) yv[q] = f2_fma(yv[q], f2_add(one2, sc[q]), sh[q]);
+                    for (int q = 0; q < PR; ++q)
+                        yv[q] = f2_fma(f2_mul(sv[i][q], rr2), f2_mul(wv[i][q], f2_add(one2, sc[q])), sh[q]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) yv[q] = f2_mul(f2_mul(sv[i][q], rr2), wv[i][q]);
                 }
                 st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(yv));
             }

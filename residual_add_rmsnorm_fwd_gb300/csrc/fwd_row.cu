@@ -206,27 +206,29 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
 #pragma unroll
                             for (int q = 0; q < PR; ++q)
                                 sv[q] = f2_fma(f2_mul(f2_add(sv[q], nm2), rr2), wv[q], bv[q]);
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < PR; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
-                        }
-                        if constexpr (ADALN) {   // y * (1 + scale) + shift
+                        } else if constexpr (ADALN) {   // (s * rrms) * (w * (1 + scale)) + shift
                             f32x2 sc[PR], sh[PR];
                             widen16<T>(scp[u][i], sc);
                             widen16<T>(shp[u][i], sh);
                             const f32x2 one2 = f2_make(1.0f, 1.0f);
 #pragma unroll
-                            for (int q = 0; q < PR; ++q) sv[q] = f2_fma(sv[q], f2_add(one2, sc[q]), sh[q]);
+                            for (int q = 0; q < PR; ++q)
+                                sv[q] = f2_fma(f2_mul(sv[q], rr2), f2_mul(wv[q], f2_add(one2, sc[q])), sh[q]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < PR; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
                         }
                         st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(sv));
                     } else {
                         float v = s_one(u, i);
                         if constexpr (LN) {
                             v = fmaf((v - mu[u]) * rrms, to_f32(wp[i].v[0]), to_f32(bp[i].v[0]));
+                        } else if constexpr (ADALN) {
+                            v = fmaf(v * rrms, to_f32(wp[i].v[0]) * (1.0f + to_f32(scp[u][i].v[0])),
+                                     to_f32(shp[u][i].v[0]));
                         } else {
                             v = (v * rrms) * to_f32(wp[i].v[0]);
                         }
-                        if constexpr (ADALN) v = fmaf(v, 1.0f + to_f32(scp[u][i].v[0]), to_f32(shp[u][i].v[0]));
                         y[base + c] = from_f32<T>(v);
                     }
                 }

@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(256) fwd_warp_kernel(FwdArgs a) {
             // row / rows_per_cond in 32 bits: both are below 2^31
             const int64_t cbase =
                 ADALN ? (int64_t)((uint32_t)row / (uint32_t)a.rows_per_cond) * a.cond_stride : 0;
-            // y = (s * rrms) * w [* (1 + scale) + shift], one rounding to the storage type
+            // y = (s * rrms) * w [AdaLN: (s * rrms) * (w * (1 + scale)) + shift], one rounding to the storage type
 #pragma unroll
             for (int k = 0; k < NPL; ++k) {
                 const int c = lane + k * 32;
@@ -107,15 +107,17 @@ __global__ void __launch_bounds__(256) fwd_warp_kernel(FwdArgs a) {
                         for (int q = 0; q < PR; ++q) sv[q] = f2_add(sv[q], rv[q]);
                     }
                     widen16<T>(a.has_w ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>()), wv);
-#pragma unroll
-                    for (int q = 0; q < PR; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
-                    if constexpr (ADALN) {
+                    if constexpr (ADALN) {   // (s * rrms) * (w * (1 + scale)) + shift
                         f32x2 sc[PR], sh[PR];
                         widen16<T>(ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC), sc);
                         widen16<T>(ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC), sh);
                         const f32x2 one2 = f2_make(1.0f, 1.0f);
 #pragma unroll
-                        for (int q = 0; q < PR; ++q) sv[q] = f2_fma(sv[q], f2_add(one2, sc[q]), sh[q]);
+                        for (int q = 0; q < PR; ++q)
+                            sv[q] = f2_fma(f2_mul(sv[q], rr2), f2_mul(wv[q], f2_add(one2, sc[q])), sh[q]);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < PR; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
                     }
                     st_global<T, VEC>(y + base + (int64_t)c * VEC, narrow16<T>(sv));
                 }
