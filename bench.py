@@ -4,7 +4,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                     [--workload step|fused_fwd|fused_fwd_bwd_residual|dit_mix|fwd_f32_small|
                                 fwd_bwd_8192|fused_f16_padded|adaln|adaln_per_token|
-                                ln_residual|ln_residual_f32]
+                                ln_residual|ln_residual_f32|long_rows]
 
 Default workload ("step"): one pass of the whole hot path on the
 (B=8, T=2048, H=4096) bf16 activations, M = 16384 rows -- the fused
@@ -202,7 +202,11 @@ class StepWorkload:
         if self.dres:   # the residual stream's incoming gradient, drawn after dy
             rng = wl.rng_for(self.c["seed"] + 100)
             self.host["dres"] = wl.matrix(rng, self.M, self.H, self.dt, self.S)
-            self.name = "fused_fwd_bwd_residual_bf16_B8xT2048xH4096" if cfg_id == 2 else self.name
+        if cfg_id == 2:
+            kind = "fused_fwd_bwd_residual" if self.dres else ("fused_fwd_bwd" if backward else "fused_fwd")
+            self.name = kind + "_bf16_B8xT2048xH4096"
+        else:
+            self.name = c["name"]
         self.kernels_per_step = 1 + (2 if backward else 0)
 
     def _make_set(self):
@@ -570,6 +574,7 @@ WORKLOADS = {
     "fused_fwd_bwd_residual": lambda: StepWorkload(2, backward=True, dres=True),
     "fwd_bwd_8192": lambda: StepWorkload(4, backward=True),
     "fused_f16_padded": lambda: StepWorkload(5, backward=True),
+    "long_rows": lambda: StepWorkload(6, backward=True),
 }
 
 

@@ -34,6 +34,7 @@ struct DevInfo {
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 std::map<std::tuple<int, const void *, int, size_t>, int> g_occ;
+std::map<std::tuple<int, const void *, int, size_t, int>, int> g_cluster_occ;
 std::map<std::pair<int, const void *>, size_t> g_smem_attr;
 
 
@@ -115,8 +116,9 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA
 // (plain and residual-fused; AdaLN and LayerNorm take the register kernel
 // there), a warp per aligned row of 512 B to 2 KB (plain, and AdaLN whose
 // conditioning rows each serve 1024 rows or more), the bulk-copy ring for
-// aligned rows of 4 KB (one input stream) or 8 KB and more, the register
-// kernel, and the two-pass chunked kernel above the register budget.
+// aligned rows of 4 KB (one input stream) or 8 KB and more up to 32 KB, the
+// register kernel, a cluster of CTAs per aligned row of 32-256 KB, and the
+// two-pass chunked kernel for the rest (longer or misaligned rows).
 int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, int sms, cudaStream_t s) {
     if (a.H < kSmallH && (mode == kPlain || mode == kResid)) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
     // AdaLN conditioning rows count as shared when each serves at least four
@@ -133,6 +135,14 @@ int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, int sms, cudaS
     if (vec && plan_fwd_ring(a.M, a.H, dtype, mode, sms, &ring))
         return to_status(launch_fwd_ring(a, dtype, mode, ring, s));
     if (fwd_row_fits(a.H, dtype, vec)) return to_status(launch_fwd_row(a, dtype, mode, vec, sms, s));
+    // aligned rows above 32 KB: a cluster of CTAs per row (the same
+    // shared-conditioning rule, with the cluster count as the row stride)
+    SplitPlan split;
+    if (vec && mode == kAdaln && plan_fwd_split(a.M, a.H, dtype, kAdalnShared, sms, &split) &&
+        (a.rows_per_cond >= 4 * (int64_t)(split.grid / split.cs) || a.rows_per_cond >= a.M))
+        return to_status(launch_fwd_split(a, dtype, kAdalnShared, split, s));
+    if (vec && plan_fwd_split(a.M, a.H, dtype, mode, sms, &split))
+        return to_status(launch_fwd_split(a, dtype, mode, split, s));
     return to_status(launch_fwd_chunked(a, dtype, mode, vec, sms, s));
 }
 
@@ -425,6 +435,124 @@ bool bwd_ring_geometry(int H, int dtype, bool dres, RingPlan *p) {
     if (smem > 200 * 1024) return false;
     finish_ring(p, nv, threads, row_bytes, streams, stages, 0);
     return true;
+}
+
+// Split-row rule: the longest segment (16-byte groups) a CTA takes, the
+// ring stages per CTA and the CTAs per SM (0 = as many as fit), by kernel.
+struct SplitRule {
+    int max_seg;
+    int stages;
+    int cps;
+};
+
+SplitRule split_rule(int streams, bool backward) {
+    if (backward) return SplitRule{2048, kBwdRingStages, 0};
+    return SplitRule{2048, 2, 0};
+}
+
+// Split-row geometry, for aligned rows above 32 KB (which one CTA's
+// registers and ring no longer hold) up to 256 KB: the smallest cluster of
+// 2, 4 or 8 CTAs whose segments fit the rule's longest segment, else eight
+// CTAs with segments up to 2048 groups (32 KB).  Groups per thread as in the
+// ring kernels for rows of the segment's length; stages from the rule,
+// fewer if the ring would exceed 200 KB of shared memory.
+bool split_geometry(int H, int dtype, int streams, bool backward, SplitPlan *p) {
+    const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
+    if (row_bytes % 16 != 0) return false;
+    const int nvec = (int)(row_bytes / 16);
+    if (nvec <= 2048) return false;   // one CTA holds the row
+    const SplitRule rule = split_rule(streams, backward);
+    int cs = 0;
+    for (int c : {2, 4, 8})
+        if (ceil_div(nvec, c) <= rule.max_seg) {
+            cs = c;
+            break;
+        }
+    if (cs == 0) {
+        if (ceil_div(nvec, 8) > 2048) return false;
+        cs = 8;
+    }
+    // seg >= 257 groups and cs * seg - nvec < cs, so the last segment is not empty
+    const int seg = ceil_div(nvec, cs);
+    const int nv = backward ? ((dtype != kF16 && seg <= 768) ? 2 : 4) : (seg <= 1024 ? 2 : 4);
+    const uint32_t pitch = (uint32_t)round_up_to(seg * 16, 128);
+    int stages = rule.stages;
+    while (stages > 2 && kRingHeaderBytes + (size_t)stages * streams * pitch > 200 * 1024) --stages;
+    const size_t smem = kRingHeaderBytes + (size_t)stages * streams * pitch;
+    if (smem > 200 * 1024 || stages > kRingMaxStages) return false;
+    p->cs = cs;
+    p->nv = nv;
+    p->threads = round_up_to(ceil_div(seg, nv), 32);
+    p->grid = 0;
+    p->max_ctas_per_sm = rule.cps;
+    p->smem_bytes = smem;
+    p->shape.stages = stages;
+    p->shape.seg_groups = seg;
+    p->shape.seg_pitch = pitch;
+    return true;
+}
+
+namespace {
+
+// Clusters of `cs` CTAs of `func` that can be resident on the device at once.
+int cluster_occupancy(const void *func, int threads, size_t smem, int cs) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const auto key = std::make_tuple(dev, func, threads, smem, cs);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_cluster_occ.find(key);
+        if (it != g_cluster_occ.end()) return it->second;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_cluster_occ[key] = n;
+    return n;
+}
+
+}  // namespace
+
+bool finish_split_plan(const void *k, int64_t M, int sm_count, SplitPlan *p) {
+    if (allow_dynamic_smem(k, p->smem_bytes) != cudaSuccess) return false;
+    int64_t nc = cluster_occupancy(k, p->threads, p->smem_bytes, p->cs);
+    if (nc <= 0) return false;
+    if (p->max_ctas_per_sm > 0) {
+        const int64_t cap = (int64_t)p->max_ctas_per_sm * sm_count / p->cs;
+        if (cap >= 1 && cap < nc) nc = cap;
+    }
+    if (nc > M) nc = M;
+    p->grid = (int)(nc * p->cs);
+    return true;
+}
+
+cudaError_t launch_cluster(const void *k, const SplitPlan &p, void **params, cudaStream_t st) {
+    cudaError_t e = allow_dynamic_smem(k, p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, k, params);
 }
 
 int occupancy(const void *func, int threads, size_t smem) {

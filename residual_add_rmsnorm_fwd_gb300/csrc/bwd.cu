@@ -346,6 +346,7 @@ const void *kernel_for_dt(const BwdPlan &p, bool vec) {
 
 const void *kernel_for(const BwdPlan &p, int dtype, bool vec) {
     if (p.kind == kBwdRing) return bwd_ring_kernel_for(dtype, p.nv, p.dres);
+    if (p.kind == kBwdSplit) return bwd_split_kernel_for(dtype, p.nv, p.dres);
     switch (dtype) {
     case kF32: return kernel_for_dt<float>(p, vec);
     case kF16: return kernel_for_dt<__half>(p, vec);
@@ -359,13 +360,26 @@ const void *kernel_for(const BwdPlan &p, int dtype, bool vec) {
 BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool dres, int sm_count) {
     BwdPlan p{};
     p.dres = dres;
+    p.cs = 1;
     RingPlan rp{};
+    SplitPlan sp{};
     if (vec && bwd_ring_geometry(H, dtype, dres, &rp)) {
         p.kind = kBwdRing;
         p.threads = rp.threads;
         p.nv = rp.nv;
         p.smem_bytes = rp.smem_bytes;
         p.ring = rp.shape;
+    } else if (vec && split_geometry(H, dtype, dres ? 3 : 2, true, &sp) &&
+               finish_split_plan(bwd_split_kernel_for(dtype, sp.nv, dres), M > 0 ? M : 1, sm_count, &sp)) {
+        p.kind = kBwdSplit;   // a cluster per row (aligned rows of 32-256 KB)
+        p.threads = sp.threads;
+        p.nv = sp.nv;
+        p.smem_bytes = sp.smem_bytes;
+        p.split = sp.shape;
+        p.cs = sp.cs;
+        p.grid = sp.grid;
+        p.partial_rows = sp.grid / sp.cs;
+        return p;
     } else {
         const int nvec = vec ? H / vec_elems(dtype) : H;
         p.kind = pick_row(nvec, vec, p.threads, p.nv) ? kBwdRow : kBwdChunked;
@@ -382,10 +396,11 @@ BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool dres, int sm_count)
         occ = occupancy(k, p.threads, smem_occ);
     const int64_t cap = (int64_t)(occ > 0 ? occ : 1) * sm_count;
     p.grid = (int)(M < cap ? (M > 0 ? M : 1) : cap);
+    p.partial_rows = p.grid;
     return p;
 }
 
-size_t bwd_partial_bytes(const BwdPlan &p, int H) { return (size_t)p.grid * (size_t)H * sizeof(float); }
+size_t bwd_partial_bytes(const BwdPlan &p, int H) { return (size_t)p.partial_rows * (size_t)H * sizeof(float); }
 
 cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, float *dweight,
                        cudaStream_t st) {
@@ -394,20 +409,33 @@ cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, 
     cudaError_t e = allow_dynamic_smem(k, p.smem_bytes);
     if (e != cudaSuccess) return e;
     BwdArgs args = a;
-    RingShape shape = p.ring;
-    size_t smem = p.smem_bytes;
-    if (p.kind == kBwdChunked && vec && a.partial != nullptr && (size_t)a.H * 4 <= kChunkedSmemAccBytes) {
-        smem = (size_t)a.H * 4;
-        args.use_smem_acc = 1;
-        e = allow_dynamic_smem(k, smem);
-        if (e != cudaSuccess) return e;
+    if (p.kind == kBwdSplit) {
+        SplitPlan sp{};
+        sp.cs = p.cs;
+        sp.nv = p.nv;
+        sp.threads = p.threads;
+        sp.grid = p.grid;
+        sp.smem_bytes = p.smem_bytes;
+        sp.shape = p.split;
+        SplitShape shape = p.split;
+        void *params[] = {&args, &shape};
+        e = launch_cluster(k, sp, params, st);
+    } else {
+        RingShape shape = p.ring;
+        size_t smem = p.smem_bytes;
+        if (p.kind == kBwdChunked && vec && a.partial != nullptr && (size_t)a.H * 4 <= kChunkedSmemAccBytes) {
+            smem = (size_t)a.H * 4;
+            args.use_smem_acc = 1;
+            e = allow_dynamic_smem(k, smem);
+            if (e != cudaSuccess) return e;
+        }
+        void *params[] = {&args, &shape};
+        e = cudaLaunchKernel(k, dim3((unsigned)p.grid), dim3((unsigned)p.threads), params, smem, st);
     }
-    void *params[] = {&args, &shape};
-    e = cudaLaunchKernel(k, dim3((unsigned)p.grid), dim3((unsigned)p.threads), params, smem, st);
     if (e != cudaSuccess) return e;
     if (dweight != nullptr && a.partial != nullptr) {
         e = launch_kernel(dweight_reduce_kernel, (unsigned)((a.H + 31) / 32), 32 * kReduceSlices, 0, st,
-                       (const float *)a.partial, p.grid, a.H, dweight);
+                       (const float *)a.partial, p.partial_rows, a.H, dweight);
     }
     return e;
 }

@@ -72,6 +72,15 @@ struct RingShape {
     uint32_t row_pitch;   // row_bytes rounded up to 128
 };
 
+// Geometry of a split-row kernel: each CTA of a cluster owns `seg_groups`
+// 16-byte groups of the row (the last CTA the rest) and stages them in a
+// ring like a whole row.
+struct SplitShape {
+    int stages;           // segments in flight per CTA (per input stream)
+    int seg_groups;       // 16-byte groups per CTA segment
+    uint32_t seg_pitch;   // seg_groups * 16 rounded up to 128
+};
+
 // Bytes reserved at the start of a ring kernel's dynamic shared memory for
 // its mbarriers (one 8-byte barrier per stage, at most 16 stages).
 constexpr int kRingHeaderBytes = 128;

@@ -48,6 +48,28 @@ struct RingPlan {
 bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p);
 bool bwd_ring_geometry(int H, int dtype, bool dres, RingPlan *p);
 
+// A split-row launch: a cluster of `cs` CTAs per row, each owning one
+// column segment; `grid` = clusters x cs.
+struct SplitPlan {
+    int cs;
+    int nv;
+    int threads;
+    int grid;
+    int max_ctas_per_sm;   // 0 = as many as fit
+    size_t smem_bytes;
+    SplitShape shape;
+};
+
+// Split geometry for aligned rows above 32 KB (false outside 32-256 KB):
+// cluster size, segment, threads, stages and shared memory, with `streams`
+// input rows per ring slot.
+bool split_geometry(int H, int dtype, int streams, bool backward, SplitPlan *p);
+// Persistent cluster count for kernel `k` (co-resident clusters, capped by
+// max_ctas_per_sm and by M); false when no cluster fits.
+bool finish_split_plan(const void *k, int64_t M, int sm_count, SplitPlan *p);
+// Launch `k` with cluster dimension p.cs.
+cudaError_t launch_cluster(const void *k, const SplitPlan &p, void **params, cudaStream_t st);
+
 // Forward launchers take the FwdMode (plain, residual-fused, AdaLN).
 // Forward with rows staged by bulk copies (16-byte aligned rows only).
 bool plan_fwd_ring(int64_t M, int H, int dtype, int mode, int sm_count, RingPlan *out);
@@ -65,22 +87,30 @@ cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, int mode, int sm_count,
 bool fwd_row_fits(int H, int dtype, bool vec);
 cudaError_t launch_fwd_row(const FwdArgs &a, int dtype, int mode, bool vec, int sm_count, cudaStream_t st);
 
+// Aligned rows above 32 KB: a cluster of CTAs per row, one segment each.
+bool plan_fwd_split(int64_t M, int H, int dtype, int mode, int sm_count, SplitPlan *out);
+cudaError_t launch_fwd_split(const FwdArgs &a, int dtype, int mode, const SplitPlan &p, cudaStream_t st);
+
 // H above the register budget: two passes over the row in chunks.
 cudaError_t launch_fwd_chunked(const FwdArgs &a, int dtype, int mode, bool vec, int sm_count, cudaStream_t st);
 
 // Backward: dx per row plus per-CTA dweight partials, then the fixed-order
 // column reduction of the partials.
-enum BwdKind { kBwdRow = 0, kBwdChunked = 1, kBwdRing = 2 };
+enum BwdKind { kBwdRow = 0, kBwdChunked = 1, kBwdRing = 2, kBwdSplit = 3 };
 struct BwdPlan {
-    int kind;        // BwdKind
-    bool dres;       // adds the residual stream's gradient (fused-forward backward)
+    int kind;          // BwdKind
+    bool dres;         // adds the residual stream's gradient (fused-forward backward)
     int threads;
-    int nv;          // 16-byte groups (or elements) per thread (row and ring kernels)
-    int grid;        // persistent CTAs = rows of the partial buffer
+    int nv;            // 16-byte groups (or elements) per thread (row, ring and split kernels)
+    int grid;          // persistent CTAs
+    int partial_rows;  // rows of the partial buffer: one per CTA, or per cluster (split)
+    int cs;            // CTAs per cluster (split kernel), else 1
     size_t smem_bytes;
     RingShape ring;
+    SplitShape split;
 };
 const void *bwd_ring_kernel_for(int dtype, int nv, bool dres);
+const void *bwd_split_kernel_for(int dtype, int nv, bool dres);
 BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool dres, int sm_count);
 size_t bwd_partial_bytes(const BwdPlan &p, int H);
 cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, float *dweight,

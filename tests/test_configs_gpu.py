@@ -1,4 +1,4 @@
-"""GPU parity on the five named workloads at full size, through the same
+"""GPU parity on the five named workloads (and the long-row case) at full size, through the same
 binding calls the benchmark times.  The oracle checks sampled rows (first,
 last and 509 seeded random rows) element by element, the full dweight (an
 fp64 sum over every row), and whole-tensor properties: every output finite,
@@ -133,3 +133,24 @@ def test_config5_fused_fwd_bwd_f16_padded(oracle):
     s_host = np.full((M, S), 0, np.uint16)
     s_host[:, :H] = gs.host()
     bwd_check(oracle, cfg, d["dy"], s_host, d["w"], gdx, dw, rows)
+
+
+def test_long_rows_fused_fwd_bwd_bf16(oracle):
+    """The long-row measurement case (bf16 4096 x 32768, 64 KB rows: the
+    split-row kernels) at full size, as the benchmark's long_rows step runs it."""
+    cfg = wl.CONFIGS[6]
+    d = wl.generate(6)
+    M, H, S, dt = cfg["M"], cfg["H"], cfg["stride"], cfg["dtype"]
+    gx, gr = Guarded(M, H, S, dt).upload(d["x"]), Guarded(M, H, S, dt).upload(d["residual"])
+    gy, gs = Guarded(M, H, S, dt), Guarded(M, H, S, dt)
+    wd = device_vec(d["w"], dt)
+    rrms = f32_buffer(M)
+    rn.rmsnorm_fwd_residual(gx.t, gr.t, wd, gy.t, gs.t, rrms, eps=cfg["eps"])
+    gdy, gdx = Guarded(M, H, S, dt).upload(d["dy"]), Guarded(M, H, S, dt)
+    dw = f32_buffer(H)
+    ws = torch.empty(rn.rmsnorm_bwd_workspace_bytes(M, H, wl.torch_dtype(dt)), dtype=torch.uint8, device="cuda")
+    rn.rmsnorm_bwd(gdy.t, gs.t, wd, rrms, gdx.t, dw, ws)
+    torch.cuda.synchronize()
+    rows = sample_rows(M)
+    fwd_check(oracle, cfg, d["x"], d["residual"], d["w"], gy, gs, rrms, rows)
+    bwd_check(oracle, cfg, d["dy"], gs.host(), d["w"], gdx, dw, rows)

@@ -36,7 +36,7 @@ def _noalloc_raw(dy, x, w, rrms, dx, dw, dtype_code):
 
 
 @pytest.mark.parametrize("dtype,M,H", [("bf16", 4099, 4096), ("f16", 2051, 6144), ("f32", 1025, 1000),
-                                       ("bf16", 3001, 64)])
+                                       ("bf16", 3001, 64), ("bf16", 301, 32768)])
 def test_noalloc_matches_workspace_backward_on_consecutive_calls(dtype, M, H):
     x, w, dy, rrms, dt = _inputs(dtype, M, H, seed=M)
     ref_dx, ref_dw = torch.empty_like(x), torch.empty(H, device="cuda")
@@ -54,7 +54,9 @@ def test_noalloc_matches_workspace_backward_on_consecutive_calls(dtype, M, H):
 
 
 def test_noalloc_rejects_oversized_partials():
-    M, H = 64, 1 << 17   # 128K columns: the partials exceed the 16 MiB array
+    # 131080 bf16 columns (rows above 256 KB take the chunked kernel, one
+    # partial row per CTA): 64 partial rows exceed the 16 MiB array
+    M, H = 64, (1 << 17) + 8
     x = torch.zeros(M, H, device="cuda", dtype=torch.bfloat16)
     w = torch.ones(H, device="cuda", dtype=torch.bfloat16)
     rrms = torch.ones(M, device="cuda")

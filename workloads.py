@@ -142,6 +142,10 @@ CONFIGS = {
     5: dict(name="fused_fwd_bwd_f16_32768x6144_stride6272", dtype="f16", M=32768, H=6144,
             stride=6272, eps=1e-5, seed=4, residual=True, weight=True, backward=True,
             save_rrms=True, outlier_frac=0.01),
+    # rows longer than one CTA holds (64 KB): the split-row (cluster) kernels;
+    # a measurement case beside the five configurations above
+    6: dict(name="fused_fwd_bwd_bf16_4096x32768", dtype="bf16", M=4096, H=32768, stride=32768, eps=1e-5,
+            seed=5, residual=True, weight=True, backward=True, save_rrms=True),
 }
 
 
