@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
                         unpack(scp[u], sc);
                         unpack(shp[u], sh);
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) v[j] = fmaf(v[j] * rrms, wv[j] * (1.0f + sc[j]), sh[j]);
+                        for (int j = 0; j < VEC; ++j) v[j] = fmaf(v[j] * rrms, fmaf(wv[j], sc[j], wv[j]), sh[j]);
                     } else {
 #pragma unroll
                         for (int j = 0; j < VEC; ++j) v[j] = (v[j] * rrms) * wv[j];

@@ -15,8 +15,9 @@
 // row is read from HBM once ("Skill: Write a Triton RMSNorm Kernel",
 // Required reasoning 3-10; Performance requirements).  AdaLN ("Rocm
 // Kernels" page, 4. AdaLN) is evaluated as (s * rrms) * (w * (1 + scale)) +
-// shift, the last multiply and add fused, in every kernel, so conditioning
-// shared by rows gives the bits of the same rows repeated: per-token
+// shift in every kernel, with w * (1 + scale) = fma(w, scale, w) (rounded
+// once) and the last multiply and add fused, so conditioning shared by rows
+// gives the bits of the same rows repeated: per-token
 // conditioning rows are staged beside x; conditioning rows shared by many
 // rows (one per sequence) are read through L1 only when the CTA's row moves
 // to another one, and kept as w * (1 + scale) and shift in registers, so a
@@ -130,9 +131,8 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                         f32x2 wt[PR], sc[PR];
                         widen16<T>(load_w(i), wt);
                         widen16<T>(ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC), sc);
-                        const f32x2 one2 = f2_make(1.0f, 1.0f);
 #pragma unroll
-                        for (int q = 0; q < PR; ++q) wv[i][q] = f2_mul(wt[q], f2_add(one2, sc[q]));
+                        for (int q = 0; q < PR; ++q) wv[i][q] = f2_fma(wt[q], sc[q], wt[q]);   // w * (1 + scale)
                         shc[i] = ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC);
                     }
                 }
@@ -224,10 +224,9 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                     f32x2 sc[PR], sh[PR];
                     widen16<T>(scp[i], sc);
                     widen16<T>(shp[i], sh);
-                    const f32x2 one2 = f2_make(1.0f, 1.0f);
 #pragma unroll
                     for (int q = 0; q < PR; ++q)
-                        yv[q] = f2_fma(f2_mul(sv[i][q], rr2), f2_mul(wv[i][q], f2_add(one2, sc[q])), sh[q]);
+                        yv[q] = f2_fma(f2_mul(sv[i][q], rr2), f2_fma(wv[i][q], sc[q], wv[i][q]), sh[q]);
                 } else {
 #pragma unroll
                     for (int q = 0; q < PR; ++q) yv[q] = f2_mul(f2_mul(sv[i][q], rr2), wv[i][q]);

@@ -124,9 +124,8 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
                         f32x2 wt[PR], sc[PR];
                         widen16<T>(load_w(i), wt);
                         widen16<T>(ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC), sc);
-                        const f32x2 one2 = f2_make(1.0f, 1.0f);
 #pragma unroll
-                        for (int q = 0; q < PR; ++q) wv[i][q] = f2_mul(wt[q], f2_add(one2, sc[q]));
+                        for (int q = 0; q < PR; ++q) wv[i][q] = f2_fma(wt[q], sc[q], wt[q]);   // w * (1 + scale)
                         shc[i] = ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC);
                     }
                 }
@@ -213,10 +212,9 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
                     f32x2 sc[PR], shv[PR];
                     widen16<T>(scp[i], sc);
                     widen16<T>(shp[i], shv);
-                    const f32x2 one2 = f2_make(1.0f, 1.0f);
 #pragma unroll
                     for (int q = 0; q < PR; ++q)
-                        yv[q] = f2_fma(f2_mul(sv[i][q], rr2), f2_mul(wv[i][q], f2_add(one2, sc[q])), shv[q]);
+                        yv[q] = f2_fma(f2_mul(sv[i][q], rr2), f2_fma(wv[i][q], sc[q], wv[i][q]), shv[q]);
                 } else {
 #pragma unroll
                     for (int q = 0; q < PR; ++q) yv[q] = f2_mul(f2_mul(sv[i][q], rr2), wv[i][q]);

@@ -111,10 +111,9 @@ __global__ void __launch_bounds__(256) fwd_warp_kernel(FwdArgs a) {
                         f32x2 sc[PR], sh[PR];
                         widen16<T>(ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC), sc);
                         widen16<T>(ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC), sh);
-                        const f32x2 one2 = f2_make(1.0f, 1.0f);
 #pragma unroll
                         for (int q = 0; q < PR; ++q)
-                            sv[q] = f2_fma(f2_mul(sv[q], rr2), f2_mul(wv[q], f2_add(one2, sc[q])), sh[q]);
+                            sv[q] = f2_fma(f2_mul(sv[q], rr2), f2_fma(wv[q], sc[q], wv[q]), sh[q]);
                     } else {
 #pragma unroll
                         for (int q = 0; q < PR; ++q) sv[q] = f2_mul(f2_mul(sv[q], rr2), wv[q]);
