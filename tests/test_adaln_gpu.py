@@ -2,8 +2,9 @@
 (register rows for H < 256 and up to the register budget, a warp per aligned
 row of 512 B to 2 KB when conditioning rows serve 1024 rows or more, the
 bulk-copy ring for aligned rows -- conditioning staged beside x, or held in
-registers when each conditioning row spans four of a CTA's row strides -- and the
-chunked two-pass kernel above), per-token and broadcast conditioning rows,
+registers when each conditioning row spans four of a CTA's row strides -- a
+cluster of CTAs per aligned row of 32-256 KB, and the chunked two-pass kernel
+for unaligned rows above the budget), per-token and broadcast conditioning rows,
 padded and misaligned layouts, in place, with guard bands around every
 buffer.
 

@@ -1,7 +1,8 @@
 """GPU parity of layernorm_fwd and layernorm_fwd_residual against the fp64
 oracle: every kernel path (the register kernel for H < 256, for rows up to the
 register budget and for unaligned rows; the bulk-copy ring for aligned rows
-of 4 KB and more (8 KB fused); the chunked kernel above the budget), with and
+of 4 KB and more (8 KB fused) up to 32 KB; a cluster of CTAs per aligned row
+of 32-256 KB; the chunked kernel for unaligned rows above the budget), with and
 without weight and bias, padded and misaligned layouts, in place, with guard
 bands around every buffer.
 

@@ -10,10 +10,12 @@ forms dx; dweight within the same rtol times sum_i |dy * xhat| per column.
 
 Kernel paths (chosen by H, dtype and layout): the lane-group kernel for
 H < 256, a warp per aligned row of 512 B to 2 KB (plain forward), the
-register-resident row kernel, the bulk-copy ring for aligned rows of 8 KB
-and more, the chunked two-pass kernel for large H; the lane-group, row and
-chunked kernels each in a 128-bit variant (16-byte aligned rows) and a
-scalar one.
+register-resident row kernel, the bulk-copy ring for aligned rows of 4-8 KB
+up to 32 KB, a thread-block cluster per aligned row of 32-256 KB (H = 32768
+bf16/f16 and f32 H = 16384 here; tests/test_split_gpu.py covers that path in
+depth), the chunked two-pass kernel for misaligned rows above the register
+budget; the lane-group, row and chunked kernels each in a 128-bit variant
+(16-byte aligned rows) and a scalar one.
 """
 import numpy as np
 import pytest
@@ -27,7 +29,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 DTYPES = ["f32", "f16", "bf16"]
-# small-H lane groups, register rows, 4097 (scalar tail), chunked two-pass
+# small-H lane groups, register rows, 4097 (scalar tail), 10001 (scalar, chunked), split rows
 H_FWD = [1, 7, 8, 64, 100, 255, 256, 1000, 1024, 2048, 4096, 4097, 6144, 8192, 10001, 16384, 32768]
 H_BWD = [1, 7, 64, 255, 256, 1000, 2048, 4096, 4097, 6144, 8192, 10001, 16384]
 
