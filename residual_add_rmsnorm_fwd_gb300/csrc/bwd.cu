@@ -246,21 +246,31 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
 }
 
 // dweight_h = sum_{b = 0}^{G-1} partial[b][h].  A CTA covers 32 columns with
-// kReduceSlices warps; warp k sums the contiguous slice of partial rows
-// [k*G/S, (k+1)*G/S) in ascending order (up to kReduceBatch loads in flight,
-// added one after another), then the slice sums are added in ascending k.
-// The order depends only on G, so the result is reproducible.
+// S warps (S = blockDim.x / 32, at most kReduceSlices); warp k sums the
+// contiguous slice of partial rows [k*G/S, (k+1)*G/S) in ascending order (up
+// to kReduceBatch loads in flight, added one after another), then the slice
+// sums are added in ascending k.  S depends only on G (reduce_slices), so the
+// order, and the result, is reproducible.
 constexpr int kReduceSlices = 32;
 constexpr int kReduceBatch = 24;
+
+// Warps per column block: about eight partial rows per slice, at most 32
+// (the usual 300-600 partial rows of the ring backward take 32; the 20-80
+// of the split backward a few, so fewer idle threads per column).
+inline int reduce_slices(int G) {
+    const int s = G / 8;
+    return s < 1 ? 1 : (s > kReduceSlices ? kReduceSlices : s);
+}
 
 __global__ void __launch_bounds__(32 * kReduceSlices)
     dweight_reduce_kernel(const float *__restrict__ partial, int G, int H, float *__restrict__ dweight) {
     __shared__ float part[kReduceSlices][33];
+    const int S = (int)(blockDim.x >> 5);
     const int col = threadIdx.x & 31, k = threadIdx.x >> 5;
     const int h = blockIdx.x * 32 + col;
     float s = 0.0f;
     if (h < H) {
-        const int g0 = (int)((int64_t)G * k / kReduceSlices), g1 = (int)((int64_t)G * (k + 1) / kReduceSlices);
+        const int g0 = (int)((int64_t)G * k / S), g1 = (int)((int64_t)G * (k + 1) / S);
         // up to kReduceBatch loads in flight per thread: a slice of the
         // usual 304-608 partial rows is one round trip to L2 (summed in
         // ascending row order either way)
@@ -277,8 +287,7 @@ __global__ void __launch_bounds__(32 * kReduceSlices)
     __syncthreads();
     if (k == 0 && h < H) {
         float t = 0.0f;
-#pragma unroll
-        for (int q = 0; q < kReduceSlices; ++q) t += part[q][col];
+        for (int q = 0; q < S; ++q) t += part[q][col];
         dweight[h] = t;
     }
 }
@@ -434,8 +443,9 @@ cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, 
     }
     if (e != cudaSuccess) return e;
     if (dweight != nullptr && a.partial != nullptr) {
-        e = launch_kernel(dweight_reduce_kernel, (unsigned)((a.H + 31) / 32), 32 * kReduceSlices, 0, st,
-                       (const float *)a.partial, p.partial_rows, a.H, dweight);
+        const unsigned threads = 32u * (unsigned)reduce_slices(p.partial_rows);
+        e = launch_kernel(dweight_reduce_kernel, (unsigned)((a.H + 31) / 32), threads, 0, st, (const float *)a.partial,
+                          p.partial_rows, a.H, dweight);
     }
     return e;
 }
