@@ -19,6 +19,18 @@ def test_algorithmic_bytes_match_the_workload_table():
     # fp16 fused forward + backward, 32768 x 6144 (padding excluded)
     f, b = bench.step_bytes(32768, 6144, 2, fused=True, weight=True, save_rrms=True, backward=True)
     assert f == 1_610_756_096 and b == 1_208_127_488
+    # long rows: bf16 fused forward + backward, 4096 x 32768 (4 and 3 row streams of 256 MiB,
+    # plus weight, rrms and, backward, the fp32 dweight)
+    f, b = bench.step_bytes(4096, 32768, 2, fused=True, weight=True, save_rrms=True, backward=True)
+    assert f == 4 * 2**28 + 65536 + 16384 and b == 3 * 2**28 + 65536 + 16384 + 131072
+
+
+def test_long_rows_workload_is_registered_with_its_configuration():
+    """The long-row workload is selectable and its configuration has the shape it measures."""
+    import workloads as wl
+    assert "long_rows" in bench.WORKLOADS
+    assert wl.CONFIGS[6]["M"] == 4096 and wl.CONFIGS[6]["H"] == 32768
+    assert wl.CONFIGS[4]["name"] == "fwd_bwd_bf16_16384x8192"
 
 
 def test_aggregate_uses_slowest_rank():
