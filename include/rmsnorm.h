@@ -161,10 +161,11 @@ int layernorm_fwd_residual(const void *x, const void *residual, const void *weig
 
 /*
  * Size in bytes of the workspace rmsnorm_bwd (and rmsnorm_bwd_residual)
- * needs for (M, H, dtype) on the current device (per-CTA binary32 dweight
- * partials).  Writes *bytes; the
- * value is fixed for a given device, M, H and dtype.  0 means no workspace
- * is needed.
+ * needs for (M, H, dtype) on the current device: binary32 dweight partials,
+ * one row of H per persistent CTA, or per cluster of CTAs for aligned rows of
+ * 32-256 KB; the largest over the layouts and the two entry points.  Writes
+ * *bytes; the value is fixed for a given device, M, H and dtype.  0 means no
+ * workspace is needed.
  */
 int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype, size_t *bytes);
 
@@ -181,9 +182,10 @@ int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype, size_t *bytes);
  *   rrms       in   M binary32 values saved by the forward (not recomputed)
  *   dx         out  M x H, row_stride
  *   dweight    out  H binary32 values, or NULL to skip it; ignored when
- *                   has_weight == 0.  Deterministic: per-CTA partial sums
- *                   over a fixed row assignment, then a fixed-order column
- *                   sum, so repeated calls on one device give identical bits.
+ *                   has_weight == 0.  Deterministic: per-CTA (or per-cluster)
+ *                   partial sums over a fixed row assignment, then a
+ *                   fixed-order column sum, so repeated calls on one device
+ *                   give identical bits.
  *   workspace  scratch of at least rmsnorm_bwd_workspace_bytes(M, H, dtype)
  *              bytes, 16-byte aligned; needed only when dweight is computed
  *              (may be NULL otherwise).  Contents on entry are ignored.
@@ -225,8 +227,10 @@ int rmsnorm_bwd_residual(const void *dy, const void *dresidual_out, const void *
  * workspace: the dweight partials live in a fixed 16 MiB array in the
  * library's device memory (held on every GPU that loads the library until
  * the process exits).  The call allocates nothing.
- *   - A shape whose partials exceed 16 MiB (rmsnorm_bwd_workspace_bytes >
- *     16 MiB) is rejected with RMSN_ERR_WORKSPACE before any launch.
+ *   - A shape whose partials, for the kernel the call selects, exceed 16 MiB
+ *     is rejected with RMSN_ERR_WORKSPACE before any launch
+ *     (rmsnorm_bwd_workspace_bytes, the largest over every layout, bounds
+ *     them from above).
  *   - The first call on a device looks up the array's device address (one
  *     cudaGetSymbolAddress with that device current); make that first call
  *     before any stream capture.
