@@ -98,3 +98,23 @@ def test_two_rank_aggregation_gloo():
         assert sorted(all_ms) == [1.5, 3.0]
         assert agg["ms"] == 3.0                                # slowest rank
         assert agg["units_per_s"] == pytest.approx(2 * 16384 / 3e-3)
+
+
+def test_reference_arm_prints_one_contract_line(capsys, monkeypatch):
+    """--impl reference times the oracle on the host (no GPU) and prints the
+    contract's JSON line; ranks other than 0 print nothing."""
+    import json
+    monkeypatch.setenv("RANK", "0")
+    bench.main(["--impl", "reference", "--workload", "fwd_f32_small", "--steps", "3", "--warmup", "3"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["higher_is_better"] is True and line["steps"] == 3 and line["warmup"] == 3
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "fwd_f32_64x1024"
+    monkeypatch.setenv("RANK", "1")
+    bench.main(["--impl", "reference", "--workload", "fwd_f32_small", "--steps", "3", "--warmup", "3"])
+    assert capsys.readouterr().out.strip() == ""
