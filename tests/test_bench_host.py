@@ -118,3 +118,13 @@ def test_reference_arm_prints_one_contract_line(capsys, monkeypatch):
     monkeypatch.setenv("RANK", "1")
     bench.main(["--impl", "reference", "--workload", "fwd_f32_small", "--steps", "3", "--warmup", "3"])
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_measured_peak_from_the_peaks_file_else_the_fallback(tmp_path, monkeypatch):
+    import json
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_peak() == (bench.FALLBACK_HBM_GBS, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6794.8}))
+    assert bench.measured_peak() == (6794.8, "measured")
+    (tmp_path / "MEASURED_PEAKS.json").write_text("{}")
+    assert bench.measured_peak()[1] == "fallback"
