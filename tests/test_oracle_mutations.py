@@ -18,7 +18,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-# (what the mistake is, text in oracle.c, its replacement); the first occurrence is replaced
+# (what the mistake is, text in oracle.c, its replacement[, which occurrence, 1-based]);
+# the first occurrence is replaced unless stated
 MUTATIONS = [
     # RMSNorm forward
     ("saved rrms inverted", "c->rrms[i] = rrms;", "c->rrms[i] = 1.0 / rrms;"),
@@ -35,6 +36,7 @@ MUTATIONS = [
     ("dx projection without rrms", "xhat * (rrms / (double)H) * dot;", "xhat * (1.0 / (double)H) * dot;"),
     ("dweight term squared", "acc[h - h0] += t;", "acc[h - h0] += t * t;"),
     ("dweight columns reversed", "acc[h - h0] += t;", "acc[h1 - 1 - h] += t;"),
+    ("dresidual_out subtracted", "c->dx[i * H + h] += d;", "c->dx[i * H + h] -= d;"),
     # storage codec
     ("f16 exponent bias", "v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
     ("truncation instead of rounding", "double q = rint(ldexp(a, (p - 1) - e));",
@@ -55,6 +57,8 @@ MUTATIONS = [
      "const double b = c->b ? load_elem(c->dtype, c->b, i % H) : 0.0;"),
     ("LayerNorm mean over H + 1", "const double mean = sum / (double)H;",
      "const double mean = sum / (double)(H + 1);"),
+    ("LayerNorm residual subtracted", "s[h] += load_elem(c->dtype, c->r, row + h);",
+     "s[h] -= load_elem(c->dtype, c->r, row + h);", 2),
     # AdaLN
     ("AdaLN without the 1 +", "* w) * (1.0 + sc);", "* w) * (sc);"),
     ("AdaLN shift subtracted", "c->y[i * H + h] = t + sh;", "c->y[i * H + h] = t - sh;"),
@@ -89,13 +93,24 @@ def test_unmutated_copy_passes_the_pins(tmp_path):
     assert rc == 0, out[-2000:]
 
 
-@pytest.mark.parametrize("what,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_fails_a_pin(tmp_path, what, old, new):
+def _replace_nth(text, old, new, n):
+    at = -1
+    for _ in range(n):
+        at = text.find(old, at + 1)
+        assert at >= 0, f"occurrence {n} of the mutation site not found in oracle.c"
+    return text[:at] + new + text[at + len(old):]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_fails_a_pin(tmp_path, mutation):
+    what, old, new = mutation[:3]
+    nth = mutation[3] if len(mutation) > 3 else 1
     tree = str(tmp_path / "tree")
     _copy_tree(tree)
     src = os.path.join(tree, "oracle", "oracle.c")
-    text = open(src).read()
-    assert old in text, f"mutation site for '{what}' not found in oracle.c"
-    open(src, "w").write(text.replace(old, new, 1))
+    with open(src) as f:
+        text = f.read()
+    with open(src, "w") as f:
+        f.write(_replace_nth(text, old, new, nth))
     rc, out = _run_pins(tree)
     assert rc != 0 and re.search(r"\d+ failed", out), f"no pin caught '{what}':\n{out[-2000:]}"
