@@ -253,6 +253,28 @@ int rmsnorm_bwd_noalloc(const void *dy, const void *x, const void *weight, const
 #define RMSN_DEVERR_PIPELINE_TIMEOUT 1u
 int rmsnorm_read_device_errors(unsigned *flags);
 
+/*
+ * Diagnostic of the failure path above, for tests of a caller's failure
+ * detection; not for production calls.  No counterpart on the pages.  Until
+ * it is called again with (0, 0), every later call of this process:
+ *   - gives each bounded pipeline wait `polls` polls (1 .. 2^22) instead of
+ *     2^22 before it reports a time-out; the one thread per CTA that issues
+ *     the copies still waits on up to 2^22 polls, so no copy is left in
+ *     flight and no barrier is re-armed early;
+ *   - with hold_first_copy == 1, makes the issuing thread of every CTA of
+ *     the bulk-copy ring kernels (16-byte aligned rows of 4-32 KB for the
+ *     plain, LayerNorm and shared-conditioning AdaLN forwards, 8-32 KB for
+ *     the residual-fused and per-token AdaLN forwards, 2-32 KB for the
+ *     backwards) wait for its first row before it has issued any copy, so
+ *     that wait runs out on purpose and sets RMSN_DEVERR_PIPELINE_TIMEOUT;
+ *     the kernel then issues its copies and finishes.
+ * Outputs of calls made under these settings are unreliable.  The settings
+ * are process-wide, not per device or stream.  Returns RMSN_ERR_INVALID for
+ * polls > 2^22, for polls == 0 with hold_first_copy != 0, or for
+ * hold_first_copy outside {0, 1}.
+ */
+int rmsnorm_debug_pipeline_timeout(unsigned polls, int hold_first_copy);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char *rmsnorm_status_string(int status);
 

@@ -25,6 +25,7 @@ __all__ = [
     "rmsnorm_fwd", "rmsnorm_fwd_residual", "rmsnorm_adaln_fwd", "layernorm_fwd", "layernorm_fwd_residual",
     "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
     "rmsnorm_bwd_residual", "rmsnorm_bwd_noalloc", "rmsnorm_read_device_errors", "rmsnorm_status_string",
+    "rmsnorm_debug_pipeline_timeout",
     "dtype_code",
 ]
 
@@ -73,6 +74,8 @@ def lib():
             L.rmsnorm_bwd_noalloc.restype = i32
             L.rmsnorm_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint)]
             L.rmsnorm_read_device_errors.restype = i32
+            L.rmsnorm_debug_pipeline_timeout.argtypes = [ctypes.c_uint, i32]
+            L.rmsnorm_debug_pipeline_timeout.restype = i32
             L.rmsnorm_status_string.argtypes = [i32]
             L.rmsnorm_status_string.restype = ctypes.c_char_p
             for f in (L.rmsnorm_fwd, L.rmsnorm_fwd_residual, L.rmsnorm_bwd_workspace_bytes, L.rmsnorm_bwd):
@@ -188,6 +191,14 @@ def rmsnorm_read_device_errors() -> int:
     out = ctypes.c_uint(0)
     _check("rmsnorm_read_device_errors", lib().rmsnorm_read_device_errors(ctypes.byref(out)))
     return out.value
+
+
+def rmsnorm_debug_pipeline_timeout(polls: int = 0, hold_first_copy: bool = False) -> None:
+    """Diagnostic of the bounded-wait failure path (see the header): every
+    later call gives its pipeline waits `polls` polls and, with
+    ``hold_first_copy``, makes each ring CTA's first wait run out on purpose.
+    ``(0, False)`` restores normal operation."""
+    _check("rmsnorm_debug_pipeline_timeout", lib().rmsnorm_debug_pipeline_timeout(int(polls), int(hold_first_copy)))
 
 
 def rmsnorm_bwd_workspace_bytes(M: int, H: int, dtype) -> int:

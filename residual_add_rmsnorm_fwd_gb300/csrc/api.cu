@@ -3,6 +3,7 @@
 // and launch.
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -33,6 +34,10 @@ struct DevInfo {
 
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
+// Pipeline-wait settings copied into every launch: the poll limit, and the
+// time-out test's held-back first copy (rmsnorm_debug_pipeline_timeout).
+std::atomic<uint32_t> g_wait_polls{kWaitPolls};
+std::atomic<int> g_hold_first{0};
 std::map<std::tuple<int, const void *, int, size_t>, int> g_occ;
 std::map<std::tuple<int, const void *, int, size_t, int>, int> g_cluster_occ;
 std::map<std::pair<int, const void *>, size_t> g_smem_attr;
@@ -191,6 +196,8 @@ int forward(const void *x, const void *residual, const void *weight, void *y, vo
 
     FwdArgs a{};
     a.err = device_error_word(dev);
+    a.wait_polls = g_wait_polls.load();
+    a.hold_first = g_hold_first.load();
     a.x = x;
     a.r = fused ? residual : nullptr;
     a.w = w;
@@ -249,6 +256,8 @@ int adaln_forward(const void *x, const void *weight, const void *scale, const vo
 
     FwdArgs a{};
     a.err = device_error_word(dev);
+    a.wait_polls = g_wait_polls.load();
+    a.hold_first = g_hold_first.load();
     a.x = x;
     a.w = w;
     a.y = y;
@@ -315,6 +324,8 @@ int layernorm_forward(const void *x, const void *residual, const void *weight, c
 
     FwdArgs a{};
     a.err = device_error_word(dev);
+    a.wait_polls = g_wait_polls.load();
+    a.hold_first = g_hold_first.load();
     a.x = x;
     a.r = r;
     a.w = w;
@@ -629,6 +640,8 @@ int backward(const void *dy, const void *dres, const void *x, const void *weight
 
     BwdArgs a{};
     a.err = device_error_word(dev);
+    a.wait_polls = g_wait_polls.load();
+    a.hold_first = g_hold_first.load();
     a.dy = dy;
     a.dres = dr;
     a.x = x;
@@ -737,6 +750,18 @@ RMSN_API int rmsnorm_read_device_errors(unsigned *flags) {
     if (cudaMemcpy(flags, word, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess ||
         cudaMemcpy(word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess)
         return RMSN_ERR_CUDA;
+    return RMSN_OK;
+}
+
+RMSN_API int rmsnorm_debug_pipeline_timeout(unsigned polls, int hold_first_copy) {
+    if (polls == 0 && hold_first_copy == 0) {   // normal operation
+        g_wait_polls.store(kWaitPolls);
+        g_hold_first.store(0);
+        return RMSN_OK;
+    }
+    if (polls == 0 || polls > kWaitPolls || (hold_first_copy != 0 && hold_first_copy != 1)) return RMSN_ERR_INVALID;
+    g_wait_polls.store(polls);
+    g_hold_first.store(hold_first_copy);
     return RMSN_OK;
 }
 

@@ -2,9 +2,17 @@
 // kernels: mbarrier set-up, expect-tx, global -> shared bulk copies with
 // byte-count completion, and a bounded wait.
 //
-// Every wait is bounded: after kWaitPolls unsuccessful polls the waiting
-// thread records kErrPipelineTimeout in the caller's device error word and
-// carries on, so barriers stay matched and the kernel always ends.
+// Every wait is bounded: a thread polls at most a limit of times, and a
+// wait still incomplete after the call's poll limit records
+// kErrPipelineTimeout in the device error word, so the kernel always ends.
+// A thread whose wait has been late once polls kWaitPollsAfterTimeout times
+// at most in its later waits, so a kernel whose pipeline has stalled ends
+// soon instead of paying the full limit on every row.  The one thread of a
+// CTA that arms a barrier (issues a stage's copies, or arms an exchange
+// barrier) reports a late wait the same way but keeps waiting, up to
+// kWaitPolls polls, so it never re-arms a barrier whose phase has not
+// completed; if even that runs out it arms nothing more (the CTA has
+// stalled).
 #pragma once
 
 #include <stdint.h>
@@ -12,6 +20,7 @@
 namespace rmsn {
 
 constexpr uint32_t kWaitPolls = 1u << 22;
+constexpr uint32_t kWaitPollsAfterTimeout = 1u << 10;
 constexpr unsigned kErrPipelineTimeout = 1u;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -60,12 +69,62 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, at most kWaitPolls polls.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned *err) {
-    for (uint32_t i = 0; i < kWaitPolls; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    if (err != nullptr) atomicOr(err, kErrPipelineTimeout);
-    return false;
+// Poll phase `parity` of `bar` at most `limit` times; returns the number of
+// polls that found it incomplete (limit: it never completed).
+__device__ __forceinline__ uint32_t mbar_poll(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    uint32_t i = 0;
+    while (i < limit && !mbar_try_wait(bar, parity)) ++i;
+    return i;
+}
+
+// Wait for phase `parity` of `bar` to complete, polling at most `limit`
+// times.  A wait still incomplete after `report` polls (report <= limit)
+// sets kErrPipelineTimeout in *err (when given) and `late`.  Returns whether
+// the phase completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, uint32_t report,
+                                          uint32_t limit, bool &late) {
+    const uint32_t n = mbar_poll(bar, parity, limit);
+    if (n >= report) {
+        late = true;
+        if (err != nullptr) atomicOr(err, kErrPipelineTimeout);
+    }
+    return n < limit;
+}
+
+// The time-out test's wait on a barrier that nothing arms yet: it runs out
+// after `polls` polls and records the time-out (out of line: it runs only
+// under the test).
+static __device__ __noinline__ void wait_unarmed(uint64_t *bar, unsigned *err, uint32_t polls) {
+    if (mbar_poll(bar, 0, polls) >= polls && err != nullptr) atomicOr(err, kErrPipelineTimeout);
+}
+
+// A wait with one limit (report == limit).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                  uint32_t polls = kWaitPolls) {
+    bool late = false;
+    return mbar_wait(bar, parity, err, polls, polls, late);
+}
+
+// Before a CTA whose issuing thread saw a wait give up exits: wait (bounded)
+// for the last issued phase of each of its `nst` stage barriers, the rows
+// 0 .. issued-1 having gone to stage k mod nst, so that no copy still lands
+// in the CTA's shared memory after it has gone.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int nst, int64_t issued) {
+    for (int j = 0; j < nst && j < issued; ++j) {
+        const int64_t uses = (issued - 1 - j) / nst + 1;
+        mbar_wait_bounded(&full[j], (uint32_t)((uses - 1) & 1), nullptr, kWaitPolls);
+    }
+}
+
+// Poll limits of a thread's next pipeline wait: `report` is the call's limit
+// (shortened once the thread has been late), `limit` the same for every
+// thread but the arming one, which waits on up to kWaitPolls until it has
+// stalled.
+__device__ __forceinline__ uint32_t wait_report(uint32_t polls, bool gave_up) {
+    return gave_up ? (polls < kWaitPollsAfterTimeout ? polls : kWaitPollsAfterTimeout) : polls;
+}
+__device__ __forceinline__ uint32_t wait_limit(uint32_t report, bool armer, bool stalled) {
+    return (armer && !stalled) ? kWaitPolls : report;
 }
 
 }  // namespace rmsn

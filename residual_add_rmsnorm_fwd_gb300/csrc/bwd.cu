@@ -25,11 +25,12 @@ template <typename T, int VEC, int NV, bool DRES>
 __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
     using P = Pack<T, VEC>;
     __shared__ float red[64];
-    const T *__restrict__ dy = static_cast<const T *>(a.dy);
-    const T *__restrict__ dres = static_cast<const T *>(a.dres);
-    const T *__restrict__ x = static_cast<const T *>(a.x);
+    // dx may be dy, x or dres itself (in-place calls): not restrict
+    const T *dy = static_cast<const T *>(a.dy);
+    const T *dres = static_cast<const T *>(a.dres);
+    const T *x = static_cast<const T *>(a.x);
     const T *__restrict__ w = static_cast<const T *>(a.w);
-    T *__restrict__ dx = static_cast<T *>(a.dx);
+    T *dx = static_cast<T *>(a.dx);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
     const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
@@ -131,11 +132,12 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
     using P = Pack<T, VEC>;
     constexpr int U = 2;
     __shared__ float red[64];
-    const T *__restrict__ dy = static_cast<const T *>(a.dy);
-    const T *__restrict__ dres = static_cast<const T *>(a.dres);
-    const T *__restrict__ x = static_cast<const T *>(a.x);
+    // dx may be dy, x or dres itself (in-place calls): not restrict
+    const T *dy = static_cast<const T *>(a.dy);
+    const T *dres = static_cast<const T *>(a.dres);
+    const T *x = static_cast<const T *>(a.x);
     const T *__restrict__ w = static_cast<const T *>(a.w);
-    T *__restrict__ dx = static_cast<T *>(a.dx);
+    T *dx = static_cast<T *>(a.dx);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
     const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
@@ -160,8 +162,8 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * blockDim.x + threadIdx.x;
                 if (c < nvec) {
-                    gp[u] = ld_cached<T, VEC>(dy + base + (int64_t)c * VEC);
-                    xp[u] = ld_cached<T, VEC>(x + base + (int64_t)c * VEC);
+                    gp[u] = ld_plain<T, VEC>(dy + base + (int64_t)c * VEC);
+                    xp[u] = ld_plain<T, VEC>(x + base + (int64_t)c * VEC);
                     wp[u] = a.has_w ? ld_cached<T, VEC>(w + (int64_t)c * VEC) : fill<T, VEC>(one<T>());
                 }
             }

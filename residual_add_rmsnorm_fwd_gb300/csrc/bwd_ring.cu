@@ -20,26 +20,31 @@
 
 namespace rmsn {
 
+// Register budget per thread: the two-group variants (up to 384 threads)
+// are held to 80 registers, so three CTAs of 256 threads fit an SM -- without
+// spills that measured fastest (78 registers against 64 with spills at four
+// CTAs: 94.5% against 93.9% of the copy peak on the default step); the other
+// variants measured fastest with ptxas's own choice.
+constexpr int bwd_ring_max_regs(int nv) { return nv == 2 ? 80 : 128; }
+
 template <typename T, int NV, bool DRES>
-// The two-group DRES variants (at most 384 threads) are held to 80
-// registers: three CTAs of 256 threads per SM without spills measured
-// fastest; the other variants measured fastest with ptxas's own choice.
-__global__ void __launch_bounds__((NV == 2 && DRES) ? 384 : 512, (NV == 2 && DRES) ? 2 : 0)
-    bwd_ring_kernel(BwdArgs a, RingShape rs) {
+__global__ void __launch_bounds__(512) __maxnreg__(bwd_ring_max_regs(NV)) bwd_ring_kernel(BwdArgs a, RingShape rs) {
     constexpr int VEC = Vec16<T>::n;
     constexpr int PR = Pairs16<T>::n;
     constexpr int NS = DRES ? 3 : 2;   // streams staged per row: dy, x (and dres)
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
+    __shared__ int64_t stall_rows;   // thread 0: rows issued before it stalled (-1: all)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     unsigned char *stages = smem + kRingHeaderBytes;
 
-    const T *__restrict__ dy = static_cast<const T *>(a.dy);
-    const T *__restrict__ dres = static_cast<const T *>(a.dres);
-    const T *__restrict__ x = static_cast<const T *>(a.x);
+    // dx may be dy, x or dres itself (in-place calls): not restrict
+    const T *dy = static_cast<const T *>(a.dy);
+    const T *dres = static_cast<const T *>(a.dres);
+    const T *x = static_cast<const T *>(a.x);
     const T *__restrict__ w = static_cast<const T *>(a.w);
-    T *__restrict__ dx = static_cast<T *>(a.dx);
+    T *dx = static_cast<T *>(a.dx);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
     const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
@@ -59,8 +64,14 @@ __global__ void __launch_bounds__((NV == 2 && DRES) ? 384 : 512, (NV == 2 && DRE
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
+        stall_rows = -1;
+        // the time-out test (hold_first): wait for row 0 before any copy is
+        // issued, so the wait runs out with nothing in flight
+        if (a.hold_first) wait_unarmed(&full[0], a.err, a.wait_polls);
     }
     __syncthreads();
+    // thread 0 issues every copy
+    bool stalled = false;   // thread 0: a copy never landed, so it issues nothing more
     if (threadIdx.x == 0)
         for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
@@ -86,7 +97,14 @@ __global__ void __launch_bounds__((NV == 2 && DRES) ? 384 : 512, (NV == 2 && DRE
         const float rr = rr_next;
         if (k + 1 < nrows) rr_next = __ldg(a.rrms + blockIdx.x + (k + 1) * G);
         const f32x2 rr2 = f2_make(rr, rr);
-        if (!mbar_wait_bounded(&full[s], phase, a.err)) gave_up = true;
+        {
+            bool late = false;
+            const uint32_t rep = wait_report(a.wait_polls, gave_up);
+            if (!mbar_wait(&full[s], phase, a.err, rep, wait_limit(rep, threadIdx.x == 0, stalled), late) &&
+                threadIdx.x == 0)
+                stalled = true;
+            gave_up |= late;
+        }
 
         P gp[NV], xp[NV], rp[NV];
         f32x2 dot2 = f2_make(0.0f, 0.0f);
@@ -113,8 +131,12 @@ __global__ void __launch_bounds__((NV == 2 && DRES) ? 384 : 512, (NV == 2 && DRE
         const float c_row = block_sum(f2_sum(dot2), red, bank) * ih;
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
-            fence_proxy_async_smem();
-            issue(k + nst, s);
+            if (!stalled) {   // thread 0 saw stage s's phase complete: refill it
+                fence_proxy_async_smem();
+                issue(k + nst, s);
+            } else if (stall_rows < 0) {
+                stall_rows = k + nst;   // rows issued before thread 0 stalled
+            }
         }
         // dx = rrms * (g - xhat * c).  With DRES it is evaluated as
         // g * rrms + (x * (-rrms^2 c) + dres), the residual stream's gradient
@@ -162,12 +184,9 @@ __global__ void __launch_bounds__((NV == 2 && DRES) ? 384 : 512, (NV == 2 && DRE
             }
         }
     }
-    if (gave_up && threadIdx.x == 0) {
-        for (int j = 0; j < nst && j < nrows; ++j) {
-            const int64_t uses = (nrows - 1 - j) / nst + 1;
-            mbar_wait_bounded(&full[j], (uint32_t)((uses - 1) & 1), nullptr);
-        }
-    }
+    // Only a stalled CTA can exit with copies in flight: thread 0 gives the
+    // last issued phase of every stage one more bounded wait.
+    if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
 }
 
 namespace {

@@ -27,15 +27,17 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
+    __shared__ int64_t stall_rows;   // thread 0: rows issued before it stalled (-1: all)
     __shared__ ClusterXchg xc;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     unsigned char *stages = smem + kRingHeaderBytes;
 
-    const T *__restrict__ dy = static_cast<const T *>(a.dy);
-    const T *__restrict__ dres = static_cast<const T *>(a.dres);
-    const T *__restrict__ x = static_cast<const T *>(a.x);
+    // dx may be dy, x or dres itself (in-place calls): not restrict
+    const T *dy = static_cast<const T *>(a.dy);
+    const T *dres = static_cast<const T *>(a.dres);
+    const T *x = static_cast<const T *>(a.x);
     const T *__restrict__ w = static_cast<const T *>(a.w);
-    T *__restrict__ dx = static_cast<T *>(a.dx);
+    T *dx = static_cast<T *>(a.dx);
     const uint32_t rank = cluster_rank(), cs = cluster_size();
     const int nvec = a.H / VEC;
     const int seg0 = (int)rank * sh.seg_groups;
@@ -60,9 +62,12 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
+        stall_rows = -1;
     }
     xchg_init(xc);
     cluster_sync();   // every CTA's exchange barriers are set up before any partial sum is sent
+    // thread 0 issues every copy and arms the exchange barriers
+    bool stalled = false;   // thread 0: a copy or partial sum never landed, so it arms nothing more
     if (threadIdx.x == 0)
         for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
@@ -87,7 +92,14 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
         const float rr = rr_next;
         if (k + 1 < nrows) rr_next = __ldg(a.rrms + ci + (k + 1) * NC);
         const f32x2 rr2 = f2_make(rr, rr);
-        if (!mbar_wait_bounded(&full[s], phase, a.err)) gave_up = true;
+        {
+            bool late = false;
+            const uint32_t rep = wait_report(a.wait_polls, gave_up);
+            if (!mbar_wait(&full[s], phase, a.err, rep, wait_limit(rep, threadIdx.x == 0, stalled), late) &&
+                threadIdx.x == 0)
+                stalled = true;
+            gave_up |= late;
+        }
 
         P gp[NV], xp[NV], rp[NV];
         f32x2 dot2 = f2_make(0.0f, 0.0f);
@@ -111,10 +123,14 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
             }
         }
         // the CTA barrier inside the reduction also frees stage s for the row nst ahead
-        const float c_row = cluster_sum(f2_sum(dot2), red, xc, nred++, rank, cs, a.err, gave_up) * ih;
+        const float c_row = cluster_sum(f2_sum(dot2), red, xc, nred++, rank, cs, a.err, a.wait_polls, gave_up, stalled) * ih;
         if (threadIdx.x == 0 && k + nst < nrows) {
-            fence_proxy_async_smem();
-            issue(k + nst, s);
+            if (!stalled) {   // thread 0 saw stage s's phase complete: refill it
+                fence_proxy_async_smem();
+                issue(k + nst, s);
+            } else if (stall_rows < 0) {
+                stall_rows = k + nst;   // rows issued before thread 0 stalled
+            }
         }
         const float kx = -(rr * rr) * c_row;
         const f32x2 kx2 = f2_make(kx, kx);
@@ -162,12 +178,9 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
             }
         }
     }
-    if (gave_up && threadIdx.x == 0) {
-        for (int j = 0; j < nst && j < nrows; ++j) {
-            const int64_t uses = (nrows - 1 - j) / nst + 1;
-            mbar_wait_bounded(&full[j], (uint32_t)((uses - 1) & 1), nullptr);
-        }
-    }
+    // Only a stalled CTA can exit with copies in flight: thread 0 gives the
+    // last issued phase of every stage one more bounded wait.
+    if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
     // no CTA leaves while another may still address its shared memory
     cluster_sync();
 }

@@ -28,6 +28,9 @@ struct FwdArgs {
     float eps;
     int has_w;
     unsigned *err;        // device error word (bounded pipeline waits report here)
+    uint32_t wait_polls;  // polls before a pipeline wait gives up (kWaitPolls unless under test)
+    int hold_first;       // test of the time-out path: each ring CTA holds back its first row
+                          // copy until its first wait has given up (0 in normal use)
     // AdaLN conditioning: token row i reads scale/shift row i / rows_per_cond
     const void *scale;
     const void *shift;
@@ -62,6 +65,8 @@ struct BwdArgs {
     int H;
     int has_w;
     unsigned *err;
+    uint32_t wait_polls;  // as in FwdArgs
+    int hold_first;       // as in FwdArgs
     int use_smem_acc;     // chunked kernel: partial row accumulated in shared memory
 };
 
@@ -116,11 +121,12 @@ template <typename T, int N> struct alignas(sizeof(T) * N) Pack {
     T v[N];
 };
 
-// Read-only streaming load: the data is not reused by this CTA, so it
-// bypasses L1 allocation (L2 still caches it).
+// Streaming load of a row the CTA reads once: no L1 allocation (L2 still
+// caches it).  A coherent load, not the non-coherent read-only path: the
+// row may be an in-place call's output, written later in the same kernel.
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
     uint4 u;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
         : "l"(p));
     return u;
@@ -139,8 +145,24 @@ __device__ __forceinline__ Pack<T, N> ld_stream(const T *p) {
     return r;
 }
 
-// Load through the read-only path with normal L1 caching (weights, reused
-// by every row a CTA handles).
+// Coherent load with normal L1 caching: a row read again soon (the chunked
+// kernels' first pass), which may be an in-place call's output.
+template <typename T, int N>
+__device__ __forceinline__ Pack<T, N> ld_plain(const T *p) {
+    Pack<T, N> r;
+    if constexpr (sizeof(T) * N == 16) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        r = *reinterpret_cast<const Pack<T, N> *>(&u);
+    } else {
+        static_assert(N == 1, "scalar path loads one element");
+        r.v[0] = p[0];
+    }
+    return r;
+}
+
+// Load through the read-only path with normal L1 caching: only for data no
+// call writes (weights, bias, AdaLN conditioning rows, saved rrms), reused by
+// every row a CTA handles.
 template <typename T, int N>
 __device__ __forceinline__ Pack<T, N> ld_cached(const T *p) {
     Pack<T, N> r;

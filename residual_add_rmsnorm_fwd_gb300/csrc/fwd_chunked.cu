@@ -23,14 +23,16 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
     using P = Pack<T, VEC>;
     constexpr int U = 2;  // vectors per thread per chunk (independent loads in flight)
     __shared__ float red[64];
-    const T *__restrict__ x = static_cast<const T *>(a.x);
-    const T *__restrict__ r = static_cast<const T *>(a.r);
+    // x and y (the residual and residual_out) may be one array (in-place
+    // calls): not restrict
+    const T *x = static_cast<const T *>(a.x);
+    const T *r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
     const T *__restrict__ bias = static_cast<const T *>(a.b);
     const T *__restrict__ scale = static_cast<const T *>(a.scale);
     const T *__restrict__ shift = static_cast<const T *>(a.shift);
-    T *__restrict__ y = static_cast<T *>(a.y);
-    T *__restrict__ s_out = static_cast<T *>(a.s_out);
+    T *y = static_cast<T *>(a.y);
+    T *s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
     const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
@@ -50,8 +52,8 @@ __global__ void __launch_bounds__(512) fwd_chunked_kernel(FwdArgs a) {
                 for (int u = 0; u < U; ++u) {
                     const int c = c0 + u * blockDim.x + threadIdx.x;
                     if (c < nvec) {
-                        xp[u] = ld_cached<T, VEC>(x + base + (int64_t)c * VEC);
-                        if constexpr (RESID) rp[u] = ld_cached<T, VEC>(r + base + (int64_t)c * VEC);
+                        xp[u] = ld_plain<T, VEC>(x + base + (int64_t)c * VEC);
+                        if constexpr (RESID) rp[u] = ld_plain<T, VEC>(r + base + (int64_t)c * VEC);
                     }
                 }
 #pragma unroll

@@ -31,8 +31,19 @@
 
 namespace rmsn {
 
+// Register budget per thread, from the measured geometry: two-group
+// kernels run up to 1024 threads per SM with one input row per slot (8 CTAs
+// of 128 at 4 KB rows, 4 of 256 at 8 KB, 2 of 512 at 16 KB) and with fused
+// LayerNorm (4 of 256 at 8 KB): 64 registers; fused RMSNorm and per-token
+// AdaLN at most 768 (2 or 3 CTAs of 256-384): 80.  Four-group kernels run
+// one CTA of up to 512 threads.
+constexpr int fwd_ring_max_regs(int nv, int mode) {
+    return nv == 2 ? ((mode == kResid || mode == kAdaln) ? 80 : 64) : 128;
+}
+
 template <typename T, int NV, int MODE>
-__global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) {
+__global__ void __launch_bounds__(512) __maxnreg__(fwd_ring_max_regs(NV, MODE))
+    fwd_ring_kernel(FwdArgs a, RingShape rs) {
     constexpr bool RESID = MODE == kResid || MODE == kLnResid;
     constexpr bool ADALN = MODE == kAdaln || MODE == kAdalnShared;
     constexpr bool LN = MODE == kLn || MODE == kLnResid;
@@ -43,17 +54,21 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
+    __shared__ int64_t stall_rows;   // thread 0: rows issued before it stalled (-1: all)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     unsigned char *stages = smem + kRingHeaderBytes;
 
-    const T *__restrict__ x = static_cast<const T *>(a.x);
-    const T *__restrict__ r = static_cast<const T *>(a.r);
+    // x and y (the residual and residual_out) may be one array (in-place
+    // calls), so they are not declared restrict; weight, bias and
+    // conditioning rows are never written by any call
+    const T *x = static_cast<const T *>(a.x);
+    const T *r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
     const T *__restrict__ scale = static_cast<const T *>(a.scale);
     const T *__restrict__ shift = static_cast<const T *>(a.shift);
     const T *__restrict__ bias = static_cast<const T *>(a.b);
-    T *__restrict__ y = static_cast<T *>(a.y);
-    T *__restrict__ s_out = static_cast<T *>(a.s_out);
+    T *y = static_cast<T *>(a.y);
+    T *s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
     const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H
@@ -78,8 +93,14 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
+        stall_rows = -1;
+        // the time-out test (hold_first): wait for row 0 before any copy is
+        // issued, so the wait runs out with nothing in flight
+        if (a.hold_first) wait_unarmed(&full[0], a.err, a.wait_polls);
     }
     __syncthreads();
+    // thread 0 issues every copy
+    bool stalled = false;   // thread 0: a copy never landed, so it issues nothing more
     if (threadIdx.x == 0)
         for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
@@ -138,7 +159,14 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
                 }
             }
         }
-        if (!mbar_wait_bounded(&full[s], phase, a.err)) gave_up = true;
+        {
+            bool late = false;
+            const uint32_t rep = wait_report(a.wait_polls, gave_up);
+            if (!mbar_wait(&full[s], phase, a.err, rep, wait_limit(rep, threadIdx.x == 0, stalled), late) &&
+                threadIdx.x == 0)
+                stalled = true;
+            gave_up |= late;
+        }
 
         // s = x (+ residual) in binary32, kept in registers for the scale step;
         // the post-add sum is written back as the next residual stream
@@ -175,8 +203,12 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
         float total = block_sum(f2_sum(ss2), red, bank);
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
-            fence_proxy_async_smem();
-            issue(k + nst, s);
+            if (!stalled) {   // thread 0 saw stage s's phase complete: refill it
+                fence_proxy_async_smem();
+                issue(k + nst, s);
+            } else if (stall_rows < 0) {
+                stall_rows = k + nst;   // rows issued before thread 0 stalled
+            }
         }
         float mu = 0.0f;
         if constexpr (LN) {   // centre the row held in registers: s <- s - mean, then its sum of squares
@@ -239,14 +271,9 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(FwdArgs a, RingShape rs) 
             phase ^= 1u;
         }
     }
-    // A copy whose wait gave up may still be landing in shared memory: give
-    // every stage's last phase one more bounded wait before the CTA exits.
-    if (gave_up && threadIdx.x == 0) {
-        for (int j = 0; j < nst && j < nrows; ++j) {
-            const int64_t uses = (nrows - 1 - j) / nst + 1;
-            mbar_wait_bounded(&full[j], (uint32_t)((uses - 1) & 1), nullptr);
-        }
-    }
+    // Only a stalled CTA can exit with copies in flight: thread 0 gives the
+    // last issued phase of every stage one more bounded wait.
+    if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
 }
 
 namespace {

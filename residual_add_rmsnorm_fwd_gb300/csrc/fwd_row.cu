@@ -27,14 +27,16 @@ __global__ void __launch_bounds__(512) fwd_row_kernel(FwdArgs a) {
     constexpr bool PAIRS = VEC > 1;
     constexpr int PR = PAIRS ? VEC / 2 : 1;
     __shared__ float red[2 * U * 32];
-    const T *__restrict__ x = static_cast<const T *>(a.x);
-    const T *__restrict__ r = static_cast<const T *>(a.r);
+    // x and y (the residual and residual_out) may be one array (in-place
+    // calls): not restrict
+    const T *x = static_cast<const T *>(a.x);
+    const T *r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
     const T *__restrict__ bias = static_cast<const T *>(a.b);
     const T *__restrict__ scale = static_cast<const T *>(a.scale);
     const T *__restrict__ shift = static_cast<const T *>(a.shift);
-    T *__restrict__ y = static_cast<T *>(a.y);
-    T *__restrict__ s_out = static_cast<T *>(a.s_out);
+    T *y = static_cast<T *>(a.y);
+    T *s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;   // exact: H < 2^24
     // the row's mean divides by H (multiplying by a per-CTA 1 / H, as the

@@ -20,11 +20,13 @@ template <typename T, int VEC, int LANES, int NPL, bool RESID, int U>
 __global__ void __launch_bounds__(256) fwd_small_kernel(FwdArgs a) {
     using P = Pack<T, VEC>;
     constexpr int RPW = 32 / LANES;  // rows per warp per slot
-    const T *__restrict__ x = static_cast<const T *>(a.x);
-    const T *__restrict__ r = static_cast<const T *>(a.r);
+    // x and y (the residual and residual_out) may be one array (in-place
+    // calls): not restrict
+    const T *x = static_cast<const T *>(a.x);
+    const T *r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
-    T *__restrict__ y = static_cast<T *>(a.y);
-    T *__restrict__ s_out = static_cast<T *>(a.s_out);
+    T *y = static_cast<T *>(a.y);
+    T *s_out = static_cast<T *>(a.s_out);
     const int nvec = a.H / VEC;
     const float hf = (float)a.H;
     const float ih = 1.0f / hf;   // one division per CTA; exact for power-of-two H

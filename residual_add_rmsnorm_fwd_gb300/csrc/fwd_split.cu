@@ -34,18 +34,21 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
+    __shared__ int64_t stall_rows;   // thread 0: rows issued before it stalled (-1: all)
     __shared__ ClusterXchg xc;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     unsigned char *stages = smem + kRingHeaderBytes;
 
-    const T *__restrict__ x = static_cast<const T *>(a.x);
-    const T *__restrict__ r = static_cast<const T *>(a.r);
+    // x and y (the residual and residual_out) may be one array (in-place
+    // calls): not restrict
+    const T *x = static_cast<const T *>(a.x);
+    const T *r = static_cast<const T *>(a.r);
     const T *__restrict__ w = static_cast<const T *>(a.w);
     const T *__restrict__ scale = static_cast<const T *>(a.scale);
     const T *__restrict__ shift = static_cast<const T *>(a.shift);
     const T *__restrict__ bias = static_cast<const T *>(a.b);
-    T *__restrict__ y = static_cast<T *>(a.y);
-    T *__restrict__ s_out = static_cast<T *>(a.s_out);
+    T *y = static_cast<T *>(a.y);
+    T *s_out = static_cast<T *>(a.s_out);
     const uint32_t rank = cluster_rank(), cs = cluster_size();
     const int nvec = a.H / VEC;
     const int seg0 = (int)rank * sh.seg_groups;                 // this CTA's first 16-byte group
@@ -75,9 +78,12 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
+        stall_rows = -1;
     }
     xchg_init(xc);
     cluster_sync();   // every CTA's exchange barriers are set up before any partial sum is sent
+    // thread 0 issues every copy and arms the exchange barriers
+    bool stalled = false;   // thread 0: a copy or partial sum never landed, so it arms nothing more
     if (threadIdx.x == 0)
         for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
@@ -131,7 +137,14 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
                 }
             }
         }
-        if (!mbar_wait_bounded(&full[s], phase, a.err)) gave_up = true;
+        {
+            bool late = false;
+            const uint32_t rep = wait_report(a.wait_polls, gave_up);
+            if (!mbar_wait(&full[s], phase, a.err, rep, wait_limit(rep, threadIdx.x == 0, stalled), late) &&
+                threadIdx.x == 0)
+                stalled = true;
+            gave_up |= late;
+        }
 
         f32x2 sv[NV][PR];
         P scp[NV], shp[NV];
@@ -163,10 +176,14 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
         }
         // the CTA barrier inside the reduction also means every thread of this
         // CTA has copied stage s out, so it can be refilled
-        float total = cluster_sum(f2_sum(ss2), red, xc, nred++, rank, cs, a.err, gave_up);
+        float total = cluster_sum(f2_sum(ss2), red, xc, nred++, rank, cs, a.err, a.wait_polls, gave_up, stalled);
         if (threadIdx.x == 0 && k + nst < nrows) {
-            fence_proxy_async_smem();
-            issue(k + nst, s);
+            if (!stalled) {   // thread 0 saw stage s's phase complete: refill it
+                fence_proxy_async_smem();
+                issue(k + nst, s);
+            } else if (stall_rows < 0) {
+                stall_rows = k + nst;   // rows issued before thread 0 stalled
+            }
         }
         float mu = 0.0f;
         if constexpr (LN) {
@@ -184,7 +201,7 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
                     }
                 }
             }
-            total = cluster_sum(f2_sum(ss2), red, xc, nred++, rank, cs, a.err, gave_up);
+            total = cluster_sum(f2_sum(ss2), red, xc, nred++, rank, cs, a.err, a.wait_polls, gave_up, stalled);
         }
         const float rrms = rsqrtf(total * ih + a.eps);
         if (rank == 0 && threadIdx.x == 0) {
@@ -227,12 +244,9 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
             phase ^= 1u;
         }
     }
-    if (gave_up && threadIdx.x == 0) {
-        for (int j = 0; j < nst && j < nrows; ++j) {
-            const int64_t uses = (nrows - 1 - j) / nst + 1;
-            mbar_wait_bounded(&full[j], (uint32_t)((uses - 1) & 1), nullptr);
-        }
-    }
+    // Only a stalled CTA can exit with copies in flight: thread 0 gives the
+    // last issued phase of every stage one more bounded wait.
+    if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
     // no CTA leaves while another may still address its shared memory
     cluster_sync();
 }

@@ -34,9 +34,16 @@ std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of this device's copy of the scratch array (looked up once).
+// A device other than an sm_103 one is refused first, with the status the
+// other entry points give, before its copy of the array is looked up.
 int scratch_for_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RMSN_ERR_UNSUPPORTED;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return RMSN_ERR_CUDA;
+    if (major != 10 || minor != 3) return RMSN_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_scratch_ptr[dev] == nullptr) {
         void *p = nullptr;
