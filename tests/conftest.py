@@ -17,3 +17,15 @@ def oracle():
     import oracle as orc
     orc.build()
     return orc
+
+
+@pytest.fixture(autouse=True)
+def device_error_word_stays_clear(request):
+    """After every GPU test: no kernel's bounded pipeline wait gave up (the
+    library's device error word reads 0; reading it also clears it)."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import residual_add_rmsnorm_fwd_gb300 as rn
+    flags = rn.rmsnorm_read_device_errors()
+    assert flags == 0, f"device error word {flags:#x}: a pipeline wait gave up during the test"

@@ -308,45 +308,88 @@ def test_partial_overlap_rejected():
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("H,offset", [(64, 0), (255, 0), (1000, 0), (2048, 0), (4096, 0), (4097, 0), (8192, 0),
-                                      (32768, 0), (4096, 1)])
-def test_in_place_matches_out_of_place(dtype, H, offset):
-    """y over x and residual_out over the residual (forward), dx over dy or over
-    dresidual_out (backward): the same bits as with separate outputs, guard
-    bands intact, on every kernel path."""
-    M = rows_for(H, 200_000)
+def check_in_place(oracle, dtype, M, H, offset, eps=1e-5):
+    """In-place calls on one kernel path, each checked against the oracle
+    element by element and bit for bit against the same call with separate
+    outputs: the fused forward with y over x and residual_out over the
+    residual; the backward with dx over dy, over x, and (fused backward) over
+    dresidual_out.  Guard bands and padding stay untouched."""
     rng = wl.rng_for(H + offset)
     xs, rs = wl.matrix(rng, M, H, dtype), wl.matrix(rng, M, H, dtype)
-    w = device_vec(wl.weight(rng, H, dtype), dtype, offset)
+    w_np = wl.weight(rng, H, dtype)
+    w = device_vec(w_np, dtype, offset)
     dys, drs = wl.matrix(rng, M, H, dtype), wl.matrix(rng, M, H, dtype)
     G = lambda a=None: Guarded(M, H, H, dtype, offset) if a is None else Guarded(M, H, H, dtype, offset).upload(a)
-    # out of place
+    # forward, out of place
     x, r, y, so = G(xs), G(rs), G(), G()
     rr = f32_buffer(M, offset)
-    rn.rmsnorm_fwd_residual(x.t, r.t, w, y.t, so.t, rr, eps=1e-5)
-    # in place
+    rn.rmsnorm_fwd_residual(x.t, r.t, w, y.t, so.t, rr, eps=eps)
+    # forward, in place
     xi, ri = G(xs), G(rs)
     rri = f32_buffer(M, offset)
-    rn.rmsnorm_fwd_residual(xi.t, ri.t, w, xi.t, ri.t, rri, eps=1e-5)
+    rn.rmsnorm_fwd_residual(xi.t, ri.t, w, xi.t, ri.t, rri, eps=eps)
     torch.cuda.synchronize()
+    ref = oracle.rmsnorm_fwd(xs, w_np, eps, dtype, residual=rs)
+    c = check_fwd_values(xi.host(), ref["y"], dtype, oracle)
+    assert c["failed"] == 0, f"in-place y: {c['failed']} failed elements"
+    want_s = oracle.encode(ref["s"], dtype)
+    assert np.array_equal(ri.host().view(want_s.dtype), want_s), "in-place residual_out not bit-exact"
+    got_rr = rri.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got_rr - ref["rrms"]) <= 1e-5 * ref["rrms"])
     assert torch.equal(xi.t, y.t) and torch.equal(ri.t, so.t) and torch.equal(rri, rr)
     assert xi.untouched_outside() and ri.untouched_outside()
 
+    # backward on the fused forward's residual_out: dx over dy, over x, over dresidual_out
+    s_np = so.host()
     nbytes = rn.rmsnorm_bwd_workspace_bytes(M, H, wl.torch_dtype(dtype))
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
     dy, dx, dw = G(dys), G(), f32_buffer(H)
     rn.rmsnorm_bwd(dy.t, so.t, w, rr, dx.t, dw, ws)
     dyi, dwi = G(dys), f32_buffer(H)
-    rn.rmsnorm_bwd(dyi.t, so.t, w, rr, dyi.t, dwi, ws)            # dx over dy
+    rn.rmsnorm_bwd(dyi.t, so.t, w, rr, dyi.t, dwi, ws)              # dx over dy
+    sx, dwx = G(s_np), f32_buffer(H)
+    rn.rmsnorm_bwd(dy.t, sx.t, w, rr, sx.t, dwx, ws)                # dx over x
     dr, dx2, dw2 = G(drs), G(), f32_buffer(H)
     rn.rmsnorm_bwd_residual(dy.t, dr.t, so.t, w, rr, dx2.t, dw2, ws)
     dri, dw2i = G(drs), f32_buffer(H)
     rn.rmsnorm_bwd_residual(dy.t, dri.t, so.t, w, rr, dri.t, dw2i, ws)   # dx over dresidual_out
     torch.cuda.synchronize()
+    rtol = bwd_rtol(dtype)
+    refb = oracle.rmsnorm_bwd(dys, s_np, w_np, eps, dtype)
+    refr = oracle.rmsnorm_bwd(dys, s_np, w_np, eps, dtype, dres=drs)
+    dec = (lambda b: b.astype(np.float64)) if dtype == "f32" else (lambda b: oracle.decode(b, dtype))
+    for name, got, want, dwt in (("dx over dy", dyi, refb, dwi), ("dx over x", sx, refb, dwx),
+                                 ("dx over dresidual_out", dri, refr, dw2i)):
+        c = check_dx(dec(got.host()), want["dx"], want["dx_scale"], rtol)
+        assert c["failed"] == 0, f"{name}: {c['failed']} failed, max rel {c['max_rel']}"
+        c = check_dweight(dwt.cpu().numpy(), want["dweight"], want["dweight_abs"], rtol)
+        assert c["failed"] == 0, f"{name}: dweight {c['failed']} failed"
+        assert got.untouched_outside()
     assert torch.equal(dyi.t, dx.t) and torch.equal(dwi, dw)
+    assert torch.equal(sx.t, dx.t) and torch.equal(dwx, dw)
     assert torch.equal(dri.t, dx2.t) and torch.equal(dw2i, dw2)
-    assert dyi.untouched_outside() and dri.untouched_outside()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("H,offset", [(64, 0), (255, 0), (1000, 0), (2048, 0), (4096, 0), (4097, 0), (8192, 0),
+                                      (32768, 0), (4096, 1)])
+def test_in_place(oracle, dtype, H, offset):
+    """In place on the lane-group, register-row, ring, split-row (H = 32768)
+    and scalar-access paths."""
+    check_in_place(oracle, dtype, rows_for(H, 200_000), H, offset)
+
+
+@pytest.mark.parametrize("dtype,H,offset,M", [
+    ("bf16", 10001, 1, 37),     # misaligned rows above the register budget: chunked forward and backward
+    ("f16", 10001, 0, 21),
+    ("f32", 65540, 0, 9),       # aligned rows above 256 KB: chunked, 16-byte accesses
+    ("bf16", 131080, 0, 7),
+    ("f32", 16384, 0, 33),      # split-row kernels (cluster per row)
+])
+def test_in_place_long_rows(oracle, dtype, H, offset, M):
+    """In place on the kernels for rows longer than one CTA holds, where a
+    row is read twice (chunked) or split over a cluster."""
+    check_in_place(oracle, dtype, M, H, offset)
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])

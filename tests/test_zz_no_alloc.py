@@ -64,3 +64,35 @@ def test_noalloc_rejects_oversized_partials():
     dx, dw = torch.empty_like(x), torch.empty(H, device="cuda")
     status = _noalloc_raw(x, x.clone(), w, rrms, dx, dw, rn.RMSN_BF16)
     assert status == 3   # RMSN_ERR_WORKSPACE, before any launch
+
+
+@pytest.mark.parametrize("has_weight,want_dw", [(0, True), (1, False)])
+def test_noalloc_without_dweight(has_weight, want_dw):
+    """No weight, or no dweight wanted: the call needs no scratch (it is not
+    looked up) and gives rmsnorm_bwd's dx, bit for bit."""
+    M, H = 1031, 4096
+    x, w, dy, rrms, dt = _inputs("bf16", M, H, seed=7)
+    ref_dx = torch.empty_like(x)
+    rn.rmsnorm_bwd(dy, x, w if has_weight else None, rrms, ref_dx, None, None)
+    dx = torch.full_like(x, float("nan"))
+    dw = torch.full((H,), 7.0, device="cuda")
+    status = rn.lib().rmsnorm_bwd_noalloc(
+        dy.data_ptr(), x.data_ptr(), w.data_ptr() if has_weight else None, rrms.data_ptr(), dx.data_ptr(),
+        dw.data_ptr() if want_dw else None, H, M, H, rn.dtype_code(dt), has_weight,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert status == 0, rn.rmsnorm_status_string(status)
+    torch.cuda.synchronize()
+    assert torch.equal(dx, ref_dx)
+    assert bool((dw == 7.0).all()), "dweight is not written when there is no weight or none is asked for"
+
+
+def test_noalloc_zero_rows_zeroes_dweight():
+    """M = 0: dweight is the empty sum (zeros); nothing else is touched."""
+    H = 4096
+    w = torch.ones(H, device="cuda", dtype=torch.bfloat16)
+    dw = torch.full((H,), 7.0, device="cuda")
+    status = rn.lib().rmsnorm_bwd_noalloc(None, None, w.data_ptr(), None, None, dw.data_ptr(), H, 0, H,
+                                          rn.RMSN_BF16, 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert status == 0, rn.rmsnorm_status_string(status)
+    torch.cuda.synchronize()
+    assert bool((dw == 0).all())
