@@ -46,6 +46,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "achieved HBM GB/s (% of GB300 peak) and rows/s for residual+RMSNorm fwd/bwd"
 NOMINAL_HBM_GBS = 8000.0
+SPREAD_REPS = 50
+L2_BYTES = 129 * 2 ** 20
+ISOLATED_LAUNCHES = 8
+ISOLATED_REPS = 20
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["residual_add_rmsnorm_fwd_gb300/csrc/*.cu", "residual_add_rmsnorm_fwd_gb300/csrc/*.cuh",
                   "residual_add_rmsnorm_fwd_gb300/csrc/*.h"]
@@ -109,7 +113,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
-    def __init__(self, gpu_index: int, period_ms: int = 50):
+    def __init__(self, gpu_index: int, period_ms: int = 10):
         self.gpu, self.period, self.proc, self.out = gpu_index, period_ms, None, None
 
     def start(self):
@@ -152,15 +156,27 @@ def parse_clock_lines(lines):
     return rows
 
 
-def summarize_clocks(rows, t0, t1):
-    inside = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05]
+def summarize_clocks(rows, t0, t1, margin=0.02):
+    """Clocks and throttle reasons of the samples taken in [t0, t1] (all
+    samples when none fell inside)."""
+    inside = [r for r in rows if t0 - margin <= r["t"] <= t1 + margin]
     use = inside if inside else rows
     if not use:
         return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
     reasons = sorted({k for r in use for k in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                                                 "sw_power_cap") if r[k]})
-    return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["sm_max"] for r in use),
-            "reasons": reasons, "samples": len(use), "in_window": bool(inside)}
+    return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_min_mhz": min(r["sm"] for r in use),
+            "sm_max_mhz": max(r["sm_max"] for r in use), "reasons": reasons, "samples": len(use),
+            "in_window": bool(inside)}
+
+
+def spread_stats(ms_per_step):
+    """Median and interquartile range of per-replay times (ms per step)."""
+    v = sorted(ms_per_step)
+    q = statistics.quantiles(v, n=4, method="inclusive") if len(v) >= 2 else [v[0]] * 3
+    return {"reps": len(v), "ms_per_step_median": round(q[1], 5), "ms_per_step_p25": round(q[0], 5),
+            "ms_per_step_p75": round(q[2], 5), "iqr_pct_of_median": round(100 * (q[2] - q[0]) / q[1], 3),
+            "ms_per_step_min": round(v[0], 5), "ms_per_step_max": round(v[-1], 5)}
 
 
 # --------------------------------------------------------------------------
@@ -678,6 +694,33 @@ def time_calls(torch, calls, stream, n_steps, graph_ok, flush=None):
     return samples
 
 
+def time_isolated(torch, calls, stream, reps=ISOLATED_REPS):
+    """Per call label: the average duration of one launch when the label's
+    calls run back to back (a CUDA graph of at least ISOLATED_LAUNCHES of
+    them, in step order, replayed `reps` times with one pair of events on
+    the launching stream around each replay): no timing node sits between
+    the launches.  Labels whose calls touch less than twice the L2 capacity
+    in all would find their operands in L2 when repeated, and are skipped."""
+    out = {}
+    for label in dict.fromkeys(c[0] for c in calls):
+        group = [c for c in calls if c[0] == label]
+        if sum(c[2] for c in group) < 2 * L2_BYTES:
+            continue
+        seq = [group[i % len(group)] for i in range(max(ISOLATED_LAUNCHES, len(group)))]
+        cap = capture_steps(torch, seq, 1, False)
+        if cap is None:
+            continue
+        g = cap[0]
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        out[label] = [a.elapsed_time(b) / len(seq) for a, b in ev]
+    return out
+
+
 def run_e2e(torch, wk, K, world):
     """ms per step end to end: every step copies its inputs from pinned host
     memory, runs the calls through the binding and copies its results back.
@@ -781,17 +824,51 @@ def run_native(args):
         if flush is not None:   # the L2 flushes are not part of the step
             flush_ms = sum(a.elapsed_time(b) for a, b in fe)
     t1 = time.time()
+    # spread: the same work replayed SPREAD_REPS more times right after the
+    # timed region, each replay between its own pair of events (clocks are
+    # sampled over both)
+    spread_ms = []
+    if graph is not None:
+        g, _, R = graph
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(SPREAD_REPS)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        spread_ms = [a.elapsed_time(b) / R for a, b in ev]
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(SPREAD_REPS)]
+        for k, (a, b) in enumerate(ev):
+            if flush is not None:
+                flush.fill_(k & 0xFF)
+            a.record(stream)
+            for _, fn, _ in calls:
+                fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        spread_ms = [a.elapsed_time(b) for a, b in ev]
+    t2 = time.time()
     barrier(world)
     ms_total = start.elapsed_time(stop) - flush_ms
     # per-kernel durations: a second pass with CUDA events around every call
     n_kernel_steps = max(1, min(K, 200))
     per_call_ms = time_calls(torch, calls, stream, n_kernel_steps, args.graph, flush)
+    isolated_ms = time_isolated(torch, calls, stream) if (args.graph and flush is None) else {}
 
     # end to end with pinned host buffers (fewer steps: host copies dominate)
     Ke = max(3, min(K, 20))
     e2e_ms = run_e2e(torch, wk, Ke, world)
 
-    clocks = summarize_clocks(sampler.stop(), t0, t1) if sampler else None
+    clock_rows = sampler.stop() if sampler else None
+    clocks = None
+    if clock_rows is not None:
+        clocks = summarize_clocks(clock_rows, t0, t2)
+        clocks["window"] = (f"timed region ({(t1 - t0) * 1e3:.1f} ms) and the {SPREAD_REPS}-replay spread pass "
+                            f"after it ({(t2 - t1) * 1e3:.1f} ms), nvidia-smi every {sampler.period} ms")
+        clocks["samples_in_timed_region"] = sum(1 for r in clock_rows if t0 <= r["t"] <= t1)
     all_ms = max_over_ranks(ms_total / K, world)
     all_e2e = max_over_ranks(e2e_ms, world)
     if rank != 0:
@@ -811,11 +888,22 @@ def run_native(args):
                        "gbs": nbytes / (avg / 1e3) / 1e9, "algorithmic_bytes": nbytes,
                        "frac_of_measured_peak": nbytes / (avg / 1e3) / 1e9 / peak,
                        "share_of_step": avg * len(idx) / (ms_total / K)}
+        if label in isolated_ms:
+            iso = statistics.median(isolated_ms[label])
+            kern[label].update(isolated_us=iso * 1e3, isolated_gbs=nbytes / (iso / 1e3) / 1e9,
+                               isolated_frac_of_measured_peak=nbytes / (iso / 1e3) / 1e9 / peak)
     dom = max(kern, key=lambda k: kern[k]["share_of_step"])
     traffic = profile_traffic(f"{dom}_{wk.dt}_{wk.M}x{wk.H}")
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(kern[dom]["gbs"], 1), "peak": peak,
-                "unit": "GB/s", "frac": round(kern[dom]["gbs"] / peak, 4), "peak_source": peak_src,
-                "traffic": traffic, "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
+    # the dominant kernel's duration: back-to-back launches without timing
+    # nodes between them when measured, else the in-step event interval (an
+    # upper bound: the events add a launch bubble)
+    d = kern[dom]
+    dom_gbs, dom_how = ((d["isolated_gbs"], f"median over {ISOLATED_REPS} replays of back-to-back launches")
+                        if "isolated_gbs" in d else (d["gbs"], "in-step CUDA-event interval (upper bound)"))
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(dom_gbs, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(dom_gbs / peak, 4), "peak_source": peak_src,
+                "traffic": traffic, "algorithmic_bytes_per_launch": d["algorithmic_bytes"], "duration": dom_how,
+                "in_step_event_frac": round(d["frac_of_measured_peak"], 4)}
     line = {
         "metric": METRIC, "value": round(agg["gbs"], 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(agg["ms"], 5), "higher_is_better": True, "scaling": "weak",
@@ -833,8 +921,14 @@ def run_native(args):
         "launch_mode": (f"CUDA graph of {graph[2]} steps replayed {K // graph[2]} times" if graph is not None
                         else "eager launches"),
         "kernel_timing": (f"{n_kernel_steps} further steps with CUDA events around every call on the launching "
-                          "stream (events add a short launch bubble, so per-kernel times are upper bounds)"),
+                          "stream (events add a short launch bubble, so per-kernel times are upper bounds); "
+                          f"isolated_*: each call label's calls back to back, a graph of at least "
+                          f"{ISOLATED_LAUNCHES} launches between one pair of events, median of {ISOLATED_REPS} "
+                          "replays (labels whose calls fit twice in L2 are not isolated)"),
         "clocks": clocks,
+        "spread": dict(spread_stats(spread_ms), steps_per_rep=(graph[2] if graph is not None else 1),
+                       what="per-replay CUDA-event time of the same steps, replayed right after the timed region"),
+        "kernel_source_hash": kernel_source_hash(),
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wk, budget_s=args.cpu_seconds)
@@ -904,6 +998,8 @@ def main(argv=None):
     ap.add_argument("--eager", dest="graph", action="store_false",
                     help="time eager launches instead of CUDA-graph replays")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--record", metavar="PATH",
+                    help="also write the JSON line, with the command that made it, to PATH")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -915,6 +1011,15 @@ def main(argv=None):
         line = run_native(args)
     if line is not None:
         print(json.dumps(line), flush=True)
+        if args.record:
+            argv_used = list(sys.argv[1:] if argv is None else argv)
+            if "--record" in argv_used:
+                i = argv_used.index("--record")
+                del argv_used[i:i + 2]
+            argv_used = [a for a in argv_used if not a.startswith("--record=")]
+            rec = dict(line, command=" ".join(["python bench.py"] + argv_used))
+            with open(args.record, "w") as f:
+                f.write(json.dumps(rec) + "\n")
 
 
 if __name__ == "__main__":
