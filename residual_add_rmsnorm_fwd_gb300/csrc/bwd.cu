@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a) {
             }
         }
     }
+    allow_dependent_launch();
 }
 
 // H above the register budget: two passes over each row with identical chunk
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(512) bwd_chunked_kernel(BwdArgs a) {
             for (int j = 0; j < VEC; j += 4)
                 *reinterpret_cast<float4 *>(prow + (int64_t)c * VEC + j) =
                     *reinterpret_cast<const float4 *>(sacc + c * VEC + j);
+    allow_dependent_launch();
 }
 
 // dweight_h = sum_{b = 0}^{G-1} partial[b][h].  A CTA covers 32 columns with
@@ -266,6 +268,9 @@ inline int reduce_slices(int G) {
 
 __global__ void __launch_bounds__(32 * kReduceSlices)
     dweight_reduce_kernel(const float *__restrict__ partial, int G, int H, float *__restrict__ dweight) {
+    // launched as a programmatic dependent of the backward: its partials are
+    // complete and visible only after this wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float part[kReduceSlices][33];
     const int S = (int)(blockDim.x >> 5);
     const int col = threadIdx.x & 31, k = threadIdx.x >> 5;
@@ -445,9 +450,23 @@ cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, 
     }
     if (e != cudaSuccess) return e;
     if (dweight != nullptr && a.partial != nullptr) {
-        const unsigned threads = 32u * (unsigned)reduce_slices(p.partial_rows);
-        e = launch_kernel(dweight_reduce_kernel, (unsigned)((a.H + 31) / 32), threads, 0, st, (const float *)a.partial,
-                          p.partial_rows, a.H, dweight);
+        // a programmatic dependent of the backward: its CTAs are scheduled as
+        // the backward's last CTAs finish (hiding the launch), and wait in
+        // griddepcontrol.wait for the backward's completion (measured: 1 us
+        // less per backward at bf16 16384 x 4096)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((a.H + 31) / 32));
+        cfg.blockDim = dim3(32u * (unsigned)reduce_slices(p.partial_rows));
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const float *part = a.partial;
+        const int G = p.partial_rows, H = a.H;
+        e = cudaLaunchKernelEx(&cfg, dweight_reduce_kernel, part, G, H, dweight);
     }
     return e;
 }

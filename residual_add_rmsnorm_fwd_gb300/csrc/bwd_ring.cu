@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(512) __maxnreg__(bwd_ring_max_regs(NV)) bwd_ri
     // Only a stalled CTA can exit with copies in flight: thread 0 gives the
     // last issued phase of every stage one more bounded wait.
     if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
+    allow_dependent_launch();
 }
 
 namespace {

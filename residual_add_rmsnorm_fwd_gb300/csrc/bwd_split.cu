@@ -13,7 +13,11 @@
 // across all rows of the cluster; at the end each CTA writes its segment of
 // the cluster's partial row, and the fixed-order column reduction over the
 // clusters' partial rows gives dweight.  The row is read from HBM once,
-// where the two-pass form for long rows reads it twice.
+// where the two-pass form for long rows reads it twice.  With DRES the dres
+// segment is not held in registers across the reduction: each thread reads
+// it from the stage while it forms dx, and the stage is refilled after a
+// CTA barrier at the end of the row (at 32 KB segments the held copy made
+// the kernel spill at 128 registers: bf16 H = 32768, 223 -> 171 us).
 #include "cluster.cuh"
 #include "launch.h"
 
@@ -101,7 +105,7 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
             gave_up |= late;
         }
 
-        P gp[NV], xp[NV], rp[NV];
+        P gp[NV], xp[NV];
         f32x2 dot2 = f2_make(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
@@ -109,7 +113,6 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
             if (c < nseg) {
                 gp[i] = *reinterpret_cast<const P *>(stage(s, 0) + (size_t)c * 16);
                 xp[i] = *reinterpret_cast<const P *>(stage(s, 1) + (size_t)c * 16);
-                if constexpr (DRES) rp[i] = *reinterpret_cast<const P *>(stage(s, 2) + (size_t)c * 16);
                 f32x2 d[PR], xv[PR], wv[PR];
                 widen16<T>(gp[i], d);
                 widen16<T>(xp[i], xv);
@@ -124,7 +127,9 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
         }
         // the CTA barrier inside the reduction also frees stage s for the row nst ahead
         const float c_row = cluster_sum(f2_sum(dot2), red, xc, nred++, rank, cs, a.err, a.wait_polls, gave_up, stalled) * ih;
-        if (threadIdx.x == 0 && k + nst < nrows) {
+        // with DRES the dres segment is read from stage s after the reduction,
+        // so the stage is refilled only after every thread has read it (below)
+        if (!DRES && threadIdx.x == 0 && k + nst < nrows) {
             if (!stalled) {   // thread 0 saw stage s's phase complete: refill it
                 fence_proxy_async_smem();
                 issue(k + nst, s);
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
                 widen16<T>(wp[i], wv);
                 if constexpr (DRES) {   // g * rrms + (x * (-rrms^2 c) + dres)
                     f32x2 rv[PR];
-                    widen16<T>(rp[i], rv);
+                    widen16<T>(*reinterpret_cast<const P *>(stage(s, 2) + (size_t)c * 16), rv);
 #pragma unroll
                     for (int q = 0; q < PR; ++q) d[q] = f2_fma(f2_mul(d[q], wv[q]), rr2, f2_fma(xv[q], kx2, rv[q]));
                 } else {                 // rrms * (g + xhat * (-c))
@@ -154,6 +159,17 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
                         d[q] = f2_mul(rr2, f2_fma(f2_mul(xv[q], rr2), nc2, f2_mul(d[q], wv[q])));
                 }
                 st_global<T, VEC>(dx + base + (int64_t)c * VEC, narrow16<T>(d));
+            }
+        }
+        if constexpr (DRES) {   // every thread has read its dres groups of stage s
+            __syncthreads();
+            if (threadIdx.x == 0 && k + nst < nrows) {
+                if (!stalled) {
+                    fence_proxy_async_smem();
+                    issue(k + nst, s);
+                } else if (stall_rows < 0) {
+                    stall_rows = k + nst;
+                }
             }
         }
         if (++s == nst) {
@@ -181,6 +197,7 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
     // Only a stalled CTA can exit with copies in flight: thread 0 gives the
     // last issued phase of every stage one more bounded wait.
     if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
+    allow_dependent_launch();
     // no CTA leaves while another may still address its shared memory
     cluster_sync();
 }

@@ -334,6 +334,16 @@ __device__ __forceinline__ Pack<T, N> fill(T v) {
     return r;
 }
 
+// Programmatic dependent launch: a grid launched after this one with
+// programmatic stream serialisation (the dweight reduction after a backward)
+// may be scheduled once every CTA of this grid has signalled or exited; it
+// still waits (griddepcontrol.wait) for this grid's completion and memory
+// before it reads anything this grid wrote.  Signalled as a CTA's last
+// step, so the dependent's CTAs only take SM slots this grid has released.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Reductions.  The xor butterfly leaves the bit-identical sum in every lane
 // (each step adds the same two values in either order), so every thread of a

@@ -16,8 +16,11 @@ inline int elem_bytes(int dtype) { return dtype == kF32 ? 4 : 2; }
 inline int vec_elems(int dtype) { return 16 / elem_bytes(dtype); }
 
 // Launch a kernel on `st` and report the launch status.  (Programmatic
-// dependent launch between consecutive kernels was measured and left out:
-// it slowed the fused forward + backward step from 0.149 to 0.164 ms.)
+// dependent launch of every kernel was measured and left out: triggered at
+// kernel entry it slowed the fused forward + backward step from 0.149 to
+// 0.164 ms; triggered at each CTA's end it gained nothing on the step and
+// lost 11% on per-sequence AdaLN.  Only the dweight reduction is launched
+// that way, after the backward.)
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*k)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
                           Args... args) {
