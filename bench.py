@@ -4,7 +4,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                     [--workload step|fused_fwd|fused_fwd_bwd_residual|dit_mix|fwd_f32_small|
                                 fwd_bwd_8192|fused_f16_padded|adaln|adaln_per_token|
-                                ln_residual|ln_residual_f32|long_rows]
+                                ln_residual|ln_residual_f32|ln_plain|long_rows]
 
 Default workload ("step"): one pass of the whole hot path on the
 (B=8, T=2048, H=4096) bf16 activations, M = 16384 rows -- the fused
@@ -499,22 +499,24 @@ class LayerNormWorkload:
     """Residual + LayerNorm forward: residual_out = x + r, y = LayerNorm(x + r)
     * w + b, on the token shape of the default step (B 8 x T 2048 x H 4096,
     bf16) or on fp32 rows of 1024 (the fp32 eval-mode setting of the page's
-    fused residual + LayerNorm).  Inputs are larger than L2; mean and rstd
-    are saved."""
+    fused residual + LayerNorm); ``fused=False``: the plain LayerNorm y =
+    LayerNorm(x) * w + b on the same shape.  Inputs are larger than L2; mean
+    and rstd are saved."""
     flush_l2 = False
 
-    def __init__(self, dtype="bf16", M=16384, H=4096):
+    def __init__(self, dtype="bf16", M=16384, H=4096, fused=True):
         import torch
         import residual_add_rmsnorm_fwd_gb300 as rn
         import workloads as wl
         self.torch, self.rn, self.wl = torch, rn, wl
         self.dt, self.M, self.H, self.S, self.eps = dtype, M, H, H, 1e-5
         self.es = wl.ELEM_BYTES[dtype]
-        self.name = f"ln_residual_{dtype}_{M}x{H}"
+        self.fused = fused
+        self.name = f"ln_{'residual' if fused else 'plain'}_{dtype}_{M}x{H}"
         rng = wl.rng_for(60)
         self.host = {"x": wl.matrix(rng, M, H, dtype), "residual": wl.matrix(rng, M, H, dtype),
                      "w": wl.weight(rng, H, dtype), "b": wl.conditioning(rng, 1, H, dtype, sigma=0.1)[0]}
-        self.bytes_per_step = 4 * M * H * self.es + 2 * H * self.es + 2 * M * 4
+        self.bytes_per_step = (4 if fused else 2) * M * H * self.es + 2 * H * self.es + 2 * M * 4
         self.rows_per_step = M
         self.kernels_per_step = 1
 
@@ -539,18 +541,23 @@ class LayerNormWorkload:
 
     def calls(self, k=0):
         rn, b = self.rn, self.sets[k]
+        if not self.fused:
+            return [("ln", lambda: rn.layernorm_fwd(b.x, self.w, self.bias, b.y, b.mean, b.rstd, eps=self.eps),
+                     self.bytes_per_step)]
         return [("ln_residual", lambda: rn.layernorm_fwd_residual(b.x, b.r, self.w, self.bias, b.y, b.s, b.mean,
                                                                   b.rstd, eps=self.eps), self.bytes_per_step)]
 
     def config(self):
-        return {"workload": self.name, "M": self.M, "H": self.H, "dtype": self.dt, "fused_residual": True,
+        return {"workload": self.name, "M": self.M, "H": self.H, "dtype": self.dt, "fused_residual": self.fused,
                 "bias": True, "eps": self.eps, "l2": "no flush: per-step working set larger than L2",
                 "algorithmic_bytes_per_step": self.bytes_per_step}
 
     def e2e_setup(self):
         torch, b = self.torch, self.sets[0]
-        self.h_in = [b.x.cpu().pin_memory(), b.r.cpu().pin_memory()]
-        self.h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (b.y, b.s)]
+        ins = [b.x, b.r] if self.fused else [b.x]
+        outs = [b.y, b.s] if self.fused else [b.y]
+        self.h_in = [t.cpu().pin_memory() for t in ins]
+        self.h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
         while len(self.sets) < 2:
             self.sets.append(self._make_set())
         self.h2d = sum(t.numel() * t.element_size() for t in self.h_in)
@@ -558,12 +565,14 @@ class LayerNormWorkload:
 
     def e2e_transfers(self, k):
         b = self.sets[k]
-        return list(zip([b.x, b.r], self.h_in)), list(zip(self.h_out, [b.y, b.s]))
+        ins = [b.x, b.r] if self.fused else [b.x]
+        outs = [b.y, b.s] if self.fused else [b.y]
+        return list(zip(ins, self.h_in)), list(zip(self.h_out, outs))
 
     def oracle_step(self, rows):
         import oracle
         oracle.layernorm_fwd(self.host["x"][:rows], self.host["w"], self.host["b"], self.eps, self.dt,
-                             residual=self.host["residual"][:rows])
+                             residual=self.host["residual"][:rows] if self.fused else None)
         return rows * self.bytes_per_step / self.M
 
 
@@ -585,6 +594,7 @@ WORKLOADS = {
     "adaln_per_token": lambda: AdalnWorkload(per_token=True),
     "ln_residual": LayerNormWorkload,
     "ln_residual_f32": lambda: LayerNormWorkload("f32", 65536, 1024),
+    "ln_plain": lambda: LayerNormWorkload(fused=False),
     "step": lambda: StepWorkload(2, backward=True),
     "fused_fwd": lambda: StepWorkload(2, backward=False),
     "fused_fwd_bwd_residual": lambda: StepWorkload(2, backward=True, dres=True),

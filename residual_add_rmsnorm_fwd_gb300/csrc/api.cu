@@ -379,7 +379,8 @@ void finish_ring(RingPlan *p, int nv, int threads, int64_t row_bytes, int stream
 }  // namespace
 
 // Forward ring geometry, measured on GB300 (bf16 unless noted, 100-540 MB
-// per call).  Two 16-byte groups per thread (four above 1024 groups).  The
+// per call).  Two 16-byte groups per thread (four above 1024 groups, and
+// for the plain norm at 4-6 KB and plain LayerNorm from 8 KB, below).  The
 // rule behind the table: about 64 KB of rows in flight per SM (stages x CTAs
 // per SM x input rows per slot x row bytes) -- less leaves HBM idle, more
 // loses DRAM efficiency -- with more CTAs per SM for short rows, whose fixed
@@ -405,22 +406,34 @@ bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
     const int streams = mode == kAdaln ? 3 : ((mode == kResid || mode == kLnResid) ? 2 : 1);
     if (row_bytes % 16 != 0 || row_bytes < (streams == 1 ? 4096 : 8192)) return false;
     const int nvec = (int)(row_bytes / 16);
-    const int nv = nvec <= 1024 ? 2 : 4;
-    const int threads = round_up_to(ceil_div(nvec, nv), 32);
-    if (threads > 512) return false;
     constexpr int64_t KB = 1024;
+    int nv = nvec <= 1024 ? 2 : 4;
     int stages = 2, cps = 2;
     if (streams == 1) {
         if (row_bytes < 6 * KB) cps = 8;
         else if (row_bytes < 8 * KB) stages = 4, cps = 4;
         else if (row_bytes < 16 * KB) cps = 4;
+        // four groups per thread where the per-row work every thread repeats
+        // dominates: the plain norm at 4-6 KB rows with three stages (bf16
+        // H = 2048: 18.0 -> 17.4 us per 12288 rows) and plain LayerNorm, with
+        // its second reduction, from 8 KB (bf16 H = 4096: 53.3 -> 49.5 us per
+        // 16384 rows); shared-conditioning AdaLN measured slower with four
+        if (mode == kPlain && row_bytes < 6 * KB) nv = 4, stages = 3;
+        if (mode == kLn && row_bytes >= 8 * KB) nv = 4;
     } else if (streams == 2) {
         if (row_bytes >= 16 * KB) cps = 1;
         else if (row_bytes >= 12 * KB) stages = 3, cps = 1;
         else if (mode == kLnResid) stages = 1, cps = 4;   // two reductions per row: more CTAs, one row each
+        // fused LayerNorm takes plain LayerNorm's four groups per thread from
+        // 8 KB (measured equal: 85.7 against 85.3 us at bf16 16384 x 4096), so
+        // the two forms sum a row in the same order and give the same bits
+        // for the same s
+        if (mode == kLnResid && row_bytes >= 8 * KB) nv = 4;
     } else {
         cps = row_bytes < 12 * KB ? 3 : 1;
     }
+    const int threads = round_up_to(ceil_div(nvec, nv), 32);
+    if (threads > 512) return false;
     if (stages > kRingMaxStages) return false;   // one mbarrier per stage in the ring header
     if (kRingHeaderBytes + (size_t)stages * streams * round_up_to((int)row_bytes, 128) > 200 * 1024) return false;
     finish_ring(p, nv, threads, row_bytes, streams, stages, cps);
@@ -431,13 +444,17 @@ bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
 // to 768 groups per row and four above (H = 4096 bf16: 256 threads; 6144:
 // 384; 8192: 256); binary16 rows take four (its widening runs on the FP32
 // pipe, and the longer per-thread chains measured faster: H = 6144 f16, 205
-// against 245 us).  Two stages, as many CTAs per SM as fit -- the backward
+// against 245 us), or three where that fills whole warps (182 us at 6144).
+// Two stages, as many CTAs per SM as fit -- the backward
 // profits from every resident warp.  Measured on GB300 at H = 4096-8192.
 bool bwd_ring_geometry(int H, int dtype, bool dres, RingPlan *p) {
     const int64_t row_bytes = (int64_t)H * elem_bytes(dtype);
     if (row_bytes % 16 != 0 || row_bytes < 2048) return false;
     const int nvec = (int)(row_bytes / 16);
-    const int nv = (dtype != kF16 && nvec <= 768) ? 2 : 4;
+    int nv = (dtype != kF16 && nvec <= 768) ? 2 : 4;
+    // binary16 rows of 768-1536 groups that split evenly into warps of three
+    // groups per thread: three (f16 H = 6144: 205.8 -> 182.2 us per 32768 rows)
+    if (dtype == kF16 && nvec >= 768 && nvec <= 1536 && nvec % 96 == 0) nv = 3;
     const int threads = round_up_to(ceil_div(nvec, nv), 32);
     if (threads > 512) return false;
     const int stages = kBwdRingStages;
