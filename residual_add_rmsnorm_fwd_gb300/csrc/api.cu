@@ -380,7 +380,7 @@ void finish_ring(RingPlan *p, int nv, int threads, int64_t row_bytes, int stream
 
 // Forward ring geometry, measured on GB300 (bf16 unless noted, 100-540 MB
 // per call).  Two 16-byte groups per thread (four above 1024 groups, and
-// for the plain norm at 4-6 KB and plain LayerNorm from 8 KB, below).  The
+// for LayerNorm from 8 KB, below).  The
 // rule behind the table: about 64 KB of rows in flight per SM (stages x CTAs
 // per SM x input rows per slot x row bytes) -- less leaves HBM idle, more
 // loses DRAM efficiency -- with more CTAs per SM for short rows, whose fixed
@@ -413,12 +413,12 @@ bool fwd_ring_geometry(int H, int dtype, int mode, RingPlan *p) {
         if (row_bytes < 6 * KB) cps = 8;
         else if (row_bytes < 8 * KB) stages = 4, cps = 4;
         else if (row_bytes < 16 * KB) cps = 4;
-        // four groups per thread where the per-row work every thread repeats
-        // dominates: the plain norm at 4-6 KB rows with three stages (bf16
-        // H = 2048: 18.0 -> 17.4 us per 12288 rows) and plain LayerNorm, with
-        // its second reduction, from 8 KB (bf16 H = 4096: 53.3 -> 49.5 us per
-        // 16384 rows); shared-conditioning AdaLN measured slower with four
-        if (mode == kPlain && row_bytes < 6 * KB) nv = 4, stages = 3;
+        // four groups per thread for plain LayerNorm from 8 KB, where the
+        // per-row work every thread repeats (two reductions) dominates (bf16
+        // H = 4096: 53.3 -> 49.5 us per 16384 rows).  At 4 KB rows four
+        // groups with three stages helped only the weighted bf16 norm (18.0
+        // -> 17.4 us per 12288 rows) and cost the unweighted, fp32 and f16
+        // ones 1-3%, and shared-conditioning AdaLN 7%: two stay there
         if (mode == kLn && row_bytes >= 8 * KB) nv = 4;
     } else if (streams == 2) {
         if (row_bytes >= 16 * KB) cps = 1;

@@ -18,7 +18,7 @@ import pytest
 
 import residual_add_rmsnorm_fwd_gb300 as rn
 import workloads as wl
-from helpers import Guarded, check_fwd_values, check_scaled_values, device_vec, f32_buffer
+from helpers import Guarded, check_scaled_values, device_vec, f32_buffer
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -127,16 +127,10 @@ def test_adaln_broadcast_is_bitwise_repeated_rows(oracle, dtype, H):
 @pytest.mark.parametrize("H", [1024, 2048, 3072, 4096, 32768])
 def test_adaln_zero_conditioning_is_bitwise_rmsnorm(oracle, dtype, H):
     """scale = shift = 0: y * (1 + 0) + 0 = y exactly, so the result equals
-    rmsnorm_fwd's bit for bit wherever both reduce a row with the same thread
-    layout.  One conditioning row serves every row, which takes the same
-    kernel family as the plain forward from H = 256 up (below that the plain
-    forward reduces a row in a lane group instead; a warp per row needs
-    conditioning rows serving 1024 rows, hence M >= 1025).  At 4-6 KB rows
-    the plain forward spreads a row over four 16-byte groups per thread and
-    shared-conditioning AdaLN over two, so their sums differ in order: there
-    both results must be within the forward tolerance of the oracle (checked
-    element by element) and their saved rrms within 1e-5 of each other
-    (the rrms tolerance)."""
+    rmsnorm_fwd's bit for bit.  One conditioning row serves every row, which
+    takes the same kernel family as the plain forward from H = 256 up (below
+    that the plain forward reduces a row in a lane group instead; a warp per
+    row needs conditioning rows serving 1024 rows, hence M >= 1025)."""
     M = max(rows_for(H), 1025)
     z = wl.to_storage(np.zeros((1, H), np.float32), dtype)
     a = run_adaln(oracle, dtype, M, H, rows_per_cond=M, sc_np=z, sh_np=z, seed=13)
@@ -147,15 +141,8 @@ def test_adaln_zero_conditioning_is_bitwise_rmsnorm(oracle, dtype, H):
     q = torch.empty(M, device="cuda")
     rn.rmsnorm_fwd(xd, wd, y, q, eps=1e-6)
     torch.cuda.synchronize()
-    row_bytes = H * wl.ELEM_BYTES[dtype]
-    if 4096 <= row_bytes < 6144:
-        ref = oracle.rmsnorm_fwd(a["x"], a["w"], 1e-6, dtype)
-        c = check_fwd_values(wl.from_torch(y, dtype), ref["y"], dtype, oracle)
-        assert c["failed"] == 0, f"plain forward: {c['failed']} elements beyond the tolerance"
-        assert torch.allclose(a["rrms"], q, rtol=1e-5, atol=0)
-    else:
-        assert torch.equal(a["gy"].t, y)
-        assert torch.equal(a["rrms"], q)
+    assert torch.equal(a["gy"].t, y)
+    assert torch.equal(a["rrms"], q)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
