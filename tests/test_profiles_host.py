@@ -44,3 +44,41 @@ def test_all_summaries_come_from_one_build():
 def test_benchmark_reads_the_step_summary():
     """The default step's dominant kernel has a summary under the label bench.py looks up."""
     assert os.path.exists(os.path.join(bench.ROOT, "profiles", "fwd_residual_bf16_16384x4096.md"))
+
+
+def _bench_line(workload):
+    path = os.path.join(bench.ROOT, "profiles", f"bench_{workload}.json")
+    assert os.path.exists(path), f"no recorded benchmark line for workload {workload}"
+    import json
+    with open(path) as f:
+        lines = [ln for ln in f.read().splitlines() if ln.strip()]
+    assert len(lines) == 1, path
+    return json.loads(lines[0])
+
+
+def test_every_workload_has_a_recorded_line_from_the_current_kernels():
+    """One JSON line per benchmark workload, written by `bench.py --record`
+    from the kernel sources as they are now."""
+    h = bench.kernel_source_hash()
+    for w in bench.WORKLOADS:
+        rec = _bench_line(w)
+        assert rec["kernel_source_hash"] == h, f"{w}: recorded from other kernel sources"
+        assert rec["command"].startswith("python bench.py") and f"--workload {w}" in rec["command"], w
+        for key in ("metric", "value", "unit", "clocks", "kernels", "roofline", "cpu_baseline", "e2e", "spread"):
+            assert key in rec, f"{w}: no {key}"
+        assert rec["metric"] == bench.METRIC
+        assert rec["clocks"]["samples"] > 0 and not set(rec["clocks"]["reasons"]) & {
+            "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}, w
+        assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1, w
+        assert 0 < rec["roofline"]["frac"] < 1.2, w
+
+
+def test_recorded_lines_are_self_consistent():
+    """value = algorithmic bytes per step / ms per step, and the roofline
+    fraction = achieved / peak, as bench.py computes them."""
+    for w in bench.WORKLOADS:
+        rec = _bench_line(w)
+        b = rec["config"]["algorithmic_bytes_per_step"]
+        assert abs(b / (rec["ms_per_step"] / 1e3) / 1e9 - rec["value"]) <= 0.01 * rec["value"], w
+        r = rec["roofline"]
+        assert abs(r["achieved"] / r["peak"] - r["frac"]) < 1e-3, w
