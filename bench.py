@@ -464,7 +464,8 @@ class AdalnWorkload:
 
     def calls(self, k=0):
         rn, b, n = self.rn, self.sets[k], self.n_sets
-        return [("adaln", lambda x=b.xs[i % n], y=b.ys[i % n], sc=b.scs[i % len(b.scs)], sh=b.shs[i % len(b.shs)]:
+        label = "adaln_per_token" if self.per_token else "adaln"
+        return [(label, lambda x=b.xs[i % n], y=b.ys[i % n], sc=b.scs[i % len(b.scs)], sh=b.shs[i % len(b.shs)]:
                  rn.rmsnorm_adaln_fwd(x, self.w, sc, sh, y, rows_per_cond=self.rpc, eps=self.eps), self.call_bytes)
                 for i in range(self.n_calls)]
 
