@@ -257,10 +257,12 @@ int rmsnorm_read_device_errors(unsigned *flags);
  * Diagnostic of the failure path above, for tests of a caller's failure
  * detection; not for production calls.  No counterpart on the pages.  Until
  * it is called again with (0, 0), every later call of this process:
- *   - gives each bounded pipeline wait `polls` polls (1 .. 2^22) instead of
- *     2^22 before it reports a time-out; the one thread per CTA that issues
- *     the copies still waits on up to 2^22 polls, so no copy is left in
- *     flight and no barrier is re-armed early;
+ *   - bounds the waits below by `polls` polls (1 .. 2^22) instead of 2^22:
+ *     the held wait (next item) always, and in the kernels that take their
+ *     wait limit from the call (binary16 storage) every wait of threads
+ *     other than the one per CTA that issues the copies, which still waits
+ *     on up to 2^22 polls, so no copy is left in flight and no barrier is
+ *     re-armed early;
  *   - with hold_first_copy == 1, makes the issuing thread of every CTA of
  *     the bulk-copy ring kernels (16-byte aligned rows of 4-32 KB for the
  *     plain, LayerNorm and shared-conditioning AdaLN forwards, 8-32 KB for

@@ -15,6 +15,7 @@
 // stalled).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace rmsn {
@@ -77,18 +78,77 @@ __device__ __forceinline__ uint32_t mbar_poll(uint64_t *bar, uint32_t parity, ui
     return i;
 }
 
-// Wait for phase `parity` of `bar` to complete, polling at most `limit`
-// times.  A wait still incomplete after `report` polls (report <= limit)
-// sets kErrPipelineTimeout in *err (when given) and `late`.  Returns whether
-// the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, uint32_t report,
-                                          uint32_t limit, bool &late) {
-    const uint32_t n = mbar_poll(bar, parity, limit);
-    if (n >= report) {
-        late = true;
-        if (err != nullptr) atomicOr(err, kErrPipelineTimeout);
+// A thread's pipeline-wait state across a kernel.  `limit` is the polls its
+// next wait may take: the call's limit, or kWaitPolls for the thread that
+// arms the barriers (issues the copies, arms an exchange); after a wait has
+// run out, kWaitPollsAfterTimeout, except that the arming thread keeps
+// kWaitPolls until a phase never completes within it (it has then stalled).
+struct PipeWait {
+    uint32_t limit;
+    bool late;      // a wait of this thread has been late (reported once)
+    bool stalled;   // the arming thread only: a phase never completed
+};
+
+__device__ __forceinline__ PipeWait pipe_wait_init(uint32_t polls, bool armer) {
+    PipeWait w;
+    w.limit = armer ? kWaitPolls : polls;
+    w.late = false;
+    w.stalled = false;
+    return w;
+}
+
+// Wait for phase `parity` of `bar`; `polls` is the call's limit (a launch
+// parameter).  Two forms with the same behaviour while `polls` is
+// kWaitPolls, the only value outside the time-out diagnostic:
+//   CONST: until a wait has run out, poll against the constant kWaitPolls
+//     (the call's limit then governs only the time-out test's held wait);
+//   else:  poll against the thread's limit held in a register, and report a
+//     wait still incomplete after `polls` polls while the arming thread
+//     waits on.
+// Which one a kernel uses is measured, not reasoned: the code around the poll
+// loop shifts the scheduling of the whole row loop.  The constant form was
+// 3 us faster for the bf16 H = 8192 backward and 4 us for plain LayerNorm at
+// bf16 16384 x 4096; the register form 6 us faster for the f16 H = 6144
+// backward and fused forward (`RING_WAIT_CONST` in the kernels).
+template <bool CONST>
+__device__ __forceinline__ void pipe_wait(uint64_t *bar, uint32_t parity, PipeWait &w, uint32_t polls, bool armer,
+                                          unsigned *err) {
+    const uint32_t short_limit = polls < kWaitPollsAfterTimeout ? polls : kWaitPollsAfterTimeout;
+    if constexpr (CONST) {
+        if (!w.late) {
+            if (mbar_poll(bar, parity, kWaitPolls) >= kWaitPolls) {
+                if (err != nullptr) atomicOr(err, kErrPipelineTimeout);
+                w.late = true;
+                w.stalled = armer;
+            }
+        } else if (mbar_poll(bar, parity, kWaitPollsAfterTimeout) >= kWaitPollsAfterTimeout) {
+            w.stalled = armer;
+        }
+    } else {
+        const uint32_t n = mbar_poll(bar, parity, w.limit);
+        if (n >= polls || n >= w.limit) {
+            if (!w.late && err != nullptr) atomicOr(err, kErrPipelineTimeout);
+            w.late = true;
+            if (!armer || n >= w.limit) {
+                if (armer) w.stalled = true;
+                w.limit = short_limit;
+            }
+        }
     }
-    return n < limit;
+}
+
+// The wait form a ring or split kernel of storage type T uses (see pipe_wait).
+template <typename T> struct RingWaitConst { static constexpr bool value = true; };
+template <> struct RingWaitConst<__half> { static constexpr bool value = false; };
+
+// Wait for phase `parity` of `bar` to complete, at most `polls` polls; a
+// wait that runs out sets kErrPipelineTimeout in *err (when given).  Returns
+// whether the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                  uint32_t polls = kWaitPolls) {
+    const uint32_t n = mbar_poll(bar, parity, polls);
+    if (n >= polls && err != nullptr) atomicOr(err, kErrPipelineTimeout);
+    return n < polls;
 }
 
 // The time-out test's wait on a barrier that nothing arms yet: it runs out
@@ -96,13 +156,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
 // under the test).
 static __device__ __noinline__ void wait_unarmed(uint64_t *bar, unsigned *err, uint32_t polls) {
     if (mbar_poll(bar, 0, polls) >= polls && err != nullptr) atomicOr(err, kErrPipelineTimeout);
-}
-
-// A wait with one limit (report == limit).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned *err,
-                                                  uint32_t polls = kWaitPolls) {
-    bool late = false;
-    return mbar_wait(bar, parity, err, polls, polls, late);
 }
 
 // Before a CTA whose issuing thread saw a wait give up exits: wait (bounded)
@@ -114,17 +167,6 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int nst, int64_t issu
         const int64_t uses = (issued - 1 - j) / nst + 1;
         mbar_wait_bounded(&full[j], (uint32_t)((uses - 1) & 1), nullptr, kWaitPolls);
     }
-}
-
-// Poll limits of a thread's next pipeline wait: `report` is the call's limit
-// (shortened once the thread has been late), `limit` the same for every
-// thread but the arming one, which waits on up to kWaitPolls until it has
-// stalled.
-__device__ __forceinline__ uint32_t wait_report(uint32_t polls, bool gave_up) {
-    return gave_up ? (polls < kWaitPollsAfterTimeout ? polls : kWaitPollsAfterTimeout) : polls;
-}
-__device__ __forceinline__ uint32_t wait_limit(uint32_t report, bool armer, bool stalled) {
-    return (armer && !stalled) ? kWaitPolls : report;
 }
 
 }  // namespace rmsn

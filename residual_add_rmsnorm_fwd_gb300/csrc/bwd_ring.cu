@@ -71,7 +71,9 @@ __global__ void __launch_bounds__(512) __maxnreg__(bwd_ring_max_regs(NV)) bwd_ri
     }
     __syncthreads();
     // thread 0 issues every copy
-    bool stalled = false;   // thread 0: a copy never landed, so it issues nothing more
+    // thread 0 arms the barriers; its waits run to kWaitPolls (see bulk.cuh)
+    const bool armer = threadIdx.x == 0;
+    PipeWait pw = pipe_wait_init(a.wait_polls, armer);
     if (threadIdx.x == 0)
         for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
@@ -86,7 +88,6 @@ __global__ void __launch_bounds__(512) __maxnreg__(bwd_ring_max_regs(NV)) bwd_ri
     }
 
     int bank = 0;
-    bool gave_up = false;
     float rr_next = __ldg(a.rrms + blockIdx.x);
     for (int64_t k = 0; k < nrows; ++k) {
         // stage s = k mod nst and its mbarrier phase (k / nst) mod 2 (nst is
@@ -97,14 +98,7 @@ __global__ void __launch_bounds__(512) __maxnreg__(bwd_ring_max_regs(NV)) bwd_ri
         const float rr = rr_next;
         if (k + 1 < nrows) rr_next = __ldg(a.rrms + blockIdx.x + (k + 1) * G);
         const f32x2 rr2 = f2_make(rr, rr);
-        {
-            bool late = false;
-            const uint32_t rep = wait_report(a.wait_polls, gave_up);
-            if (!mbar_wait(&full[s], phase, a.err, rep, wait_limit(rep, threadIdx.x == 0, stalled), late) &&
-                threadIdx.x == 0)
-                stalled = true;
-            gave_up |= late;
-        }
+        pipe_wait<RingWaitConst<T>::value>(&full[s], phase, pw, a.wait_polls, armer, a.err);
 
         P gp[NV], xp[NV], rp[NV];
         f32x2 dot2 = f2_make(0.0f, 0.0f);
@@ -131,7 +125,7 @@ __global__ void __launch_bounds__(512) __maxnreg__(bwd_ring_max_regs(NV)) bwd_ri
         const float c_row = block_sum(f2_sum(dot2), red, bank) * ih;
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
-            if (!stalled) {   // thread 0 saw stage s's phase complete: refill it
+            if (!pw.stalled) {   // thread 0 saw stage s's phase complete: refill it
                 fence_proxy_async_smem();
                 issue(k + nst, s);
             } else if (stall_rows < 0) {
@@ -186,7 +180,7 @@ __global__ void __launch_bounds__(512) __maxnreg__(bwd_ring_max_regs(NV)) bwd_ri
     }
     // Only a stalled CTA can exit with copies in flight: thread 0 gives the
     // last issued phase of every stage one more bounded wait.
-    if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
+    if (pw.stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
     allow_dependent_launch();
 }
 

@@ -71,7 +71,9 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
     xchg_init(xc);
     cluster_sync();   // every CTA's exchange barriers are set up before any partial sum is sent
     // thread 0 issues every copy and arms the exchange barriers
-    bool stalled = false;   // thread 0: a copy or partial sum never landed, so it arms nothing more
+    // thread 0 arms the barriers; its waits run to kWaitPolls (see bulk.cuh)
+    const bool armer = threadIdx.x == 0;
+    PipeWait pw = pipe_wait_init(a.wait_polls, armer);
     if (threadIdx.x == 0)
         for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
@@ -86,7 +88,6 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
     }
 
     uint32_t nred = 0;   // cluster reductions so far
-    bool gave_up = false;
     float rr_next = __ldg(a.rrms + ci);
     // stage s = k mod nst and its mbarrier phase (k / nst) mod 2, advanced per row
     int s = 0;
@@ -96,14 +97,7 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
         const float rr = rr_next;
         if (k + 1 < nrows) rr_next = __ldg(a.rrms + ci + (k + 1) * NC);
         const f32x2 rr2 = f2_make(rr, rr);
-        {
-            bool late = false;
-            const uint32_t rep = wait_report(a.wait_polls, gave_up);
-            if (!mbar_wait(&full[s], phase, a.err, rep, wait_limit(rep, threadIdx.x == 0, stalled), late) &&
-                threadIdx.x == 0)
-                stalled = true;
-            gave_up |= late;
-        }
+        pipe_wait<RingWaitConst<T>::value>(&full[s], phase, pw, a.wait_polls, armer, a.err);
 
         P gp[NV], xp[NV];
         f32x2 dot2 = f2_make(0.0f, 0.0f);
@@ -126,11 +120,11 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
             }
         }
         // the CTA barrier inside the reduction also frees stage s for the row nst ahead
-        const float c_row = cluster_sum(f2_sum(dot2), red, xc, nred++, rank, cs, a.err, a.wait_polls, gave_up, stalled) * ih;
+        const float c_row = cluster_sum<RingWaitConst<T>::value>(f2_sum(dot2), red, xc, nred++, rank, cs, a.err, a.wait_polls, armer, pw) * ih;
         // with DRES the dres segment is read from stage s after the reduction,
         // so the stage is refilled only after every thread has read it (below)
         if (!DRES && threadIdx.x == 0 && k + nst < nrows) {
-            if (!stalled) {   // thread 0 saw stage s's phase complete: refill it
+            if (!pw.stalled) {   // thread 0 saw stage s's phase complete: refill it
                 fence_proxy_async_smem();
                 issue(k + nst, s);
             } else if (stall_rows < 0) {
@@ -164,7 +158,7 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
         if constexpr (DRES) {   // every thread has read its dres groups of stage s
             __syncthreads();
             if (threadIdx.x == 0 && k + nst < nrows) {
-                if (!stalled) {
+                if (!pw.stalled) {
                     fence_proxy_async_smem();
                     issue(k + nst, s);
                 } else if (stall_rows < 0) {
@@ -196,7 +190,7 @@ __global__ void __launch_bounds__(512) bwd_split_kernel(BwdArgs a, SplitShape sh
     }
     // Only a stalled CTA can exit with copies in flight: thread 0 gives the
     // last issued phase of every stage one more bounded wait.
-    if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
+    if (pw.stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
     allow_dependent_launch();
     // no CTA leaves while another may still address its shared memory
     cluster_sync();

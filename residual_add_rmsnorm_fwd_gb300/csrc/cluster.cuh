@@ -94,18 +94,17 @@ __device__ __forceinline__ void xchg_init(ClusterXchg &xc) {
 // used again by reduction j + 2, which another CTA can start only after this
 // CTA has sent its partial of reduction j + 1, i.e. after it has read the
 // slots of reduction j.  The wait is bounded: a wait still incomplete after
-// `polls` polls (fewer once the thread has been late) records
-// kErrPipelineTimeout in *err and sets gave_up; thread 0, which arms the
-// barrier, waits on up to kWaitPolls so that it never re-arms an incomplete
-// phase, and arms nothing more (stalled) if even that runs out.
+// `polls` polls records kErrPipelineTimeout in *err (pipe_wait); the arming
+// thread (thread 0) waits on up to kWaitPolls so that it never re-arms an
+// incomplete phase, and arms nothing more (stalled) if even that runs out.
+template <bool WAIT_CONST>
 __device__ __forceinline__ float cluster_sum(float v, float *red, ClusterXchg &xc, uint32_t j, uint32_t rank,
-                                             uint32_t cs, unsigned *err, uint32_t polls, bool &gave_up,
-                                             bool &stalled) {
+                                             uint32_t cs, unsigned *err, uint32_t polls, bool armer, PipeWait &pw) {
     const int b = (int)(j & 1u);
     const float t = block_sum(v, red, b);
-    if (threadIdx.x == 0) {
+    if (armer) {
         xc.slot[b][rank] = t;
-        if (!stalled) {
+        if (!pw.stalled) {
             mbar_arrive_expect_tx(&xc.bar[b], (cs - 1) * 4u);
             for (uint32_t q = 1; q < cs; ++q) {
                 const uint32_t peer = (rank + q) & (cs - 1);   // cs is 2, 4 or 8
@@ -113,12 +112,7 @@ __device__ __forceinline__ float cluster_sum(float v, float *red, ClusterXchg &x
             }
         }
     }
-    bool late = false;
-    const uint32_t rep = wait_report(polls, gave_up);
-    if (!mbar_wait(&xc.bar[b], (j >> 1) & 1u, err, rep, wait_limit(rep, threadIdx.x == 0, stalled), late) &&
-        threadIdx.x == 0)
-        stalled = true;
-    gave_up |= late;
+    pipe_wait<WAIT_CONST>(&xc.bar[b], (j >> 1) & 1u, pw, polls, armer, err);
     float total = 0.0f;
     for (uint32_t q = 0; q < cs; ++q) total += xc.slot[b][q];
     return total;

@@ -100,7 +100,9 @@ __global__ void __launch_bounds__(512) __maxnreg__(fwd_ring_max_regs(NV, MODE))
     }
     __syncthreads();
     // thread 0 issues every copy
-    bool stalled = false;   // thread 0: a copy never landed, so it issues nothing more
+    // thread 0 arms the barriers; its waits run to kWaitPolls (see bulk.cuh)
+    const bool armer = threadIdx.x == 0;
+    PipeWait pw = pipe_wait_init(a.wait_polls, armer);
     if (threadIdx.x == 0)
         for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
@@ -130,7 +132,6 @@ __global__ void __launch_bounds__(512) __maxnreg__(fwd_ring_max_regs(NV, MODE))
     }
 
     int bank = 0;
-    bool gave_up = false;
     // stage s = k mod nst and its mbarrier phase = (k / nst) mod 2, advanced
     // per row (no division in the loop)
     int s = 0;
@@ -159,14 +160,7 @@ __global__ void __launch_bounds__(512) __maxnreg__(fwd_ring_max_regs(NV, MODE))
                 }
             }
         }
-        {
-            bool late = false;
-            const uint32_t rep = wait_report(a.wait_polls, gave_up);
-            if (!mbar_wait(&full[s], phase, a.err, rep, wait_limit(rep, threadIdx.x == 0, stalled), late) &&
-                threadIdx.x == 0)
-                stalled = true;
-            gave_up |= late;
-        }
+        pipe_wait<RingWaitConst<T>::value>(&full[s], phase, pw, a.wait_polls, armer, a.err);
 
         // s = x (+ residual) in binary32, kept in registers for the scale step;
         // the post-add sum is written back as the next residual stream
@@ -203,7 +197,7 @@ __global__ void __launch_bounds__(512) __maxnreg__(fwd_ring_max_regs(NV, MODE))
         float total = block_sum(f2_sum(ss2), red, bank);
         bank ^= 1;
         if (threadIdx.x == 0 && k + nst < nrows) {
-            if (!stalled) {   // thread 0 saw stage s's phase complete: refill it
+            if (!pw.stalled) {   // thread 0 saw stage s's phase complete: refill it
                 fence_proxy_async_smem();
                 issue(k + nst, s);
             } else if (stall_rows < 0) {
@@ -273,7 +267,7 @@ __global__ void __launch_bounds__(512) __maxnreg__(fwd_ring_max_regs(NV, MODE))
     }
     // Only a stalled CTA can exit with copies in flight: thread 0 gives the
     // last issued phase of every stage one more bounded wait.
-    if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
+    if (pw.stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
 }
 
 namespace {

@@ -83,7 +83,9 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
     xchg_init(xc);
     cluster_sync();   // every CTA's exchange barriers are set up before any partial sum is sent
     // thread 0 issues every copy and arms the exchange barriers
-    bool stalled = false;   // thread 0: a copy or partial sum never landed, so it arms nothing more
+    // thread 0 arms the barriers; its waits run to kWaitPolls (see bulk.cuh)
+    const bool armer = threadIdx.x == 0;
+    PipeWait pw = pipe_wait_init(a.wait_polls, armer);
     if (threadIdx.x == 0)
         for (int k = 0; k < nst && k < nrows; ++k) issue(k, k);
 
@@ -112,7 +114,6 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
     }
 
     uint32_t nred = 0;   // cluster reductions so far
-    bool gave_up = false;
     int s = 0;
     uint32_t phase = 0;
     for (int64_t k = 0; k < nrows; ++k) {
@@ -137,14 +138,7 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
                 }
             }
         }
-        {
-            bool late = false;
-            const uint32_t rep = wait_report(a.wait_polls, gave_up);
-            if (!mbar_wait(&full[s], phase, a.err, rep, wait_limit(rep, threadIdx.x == 0, stalled), late) &&
-                threadIdx.x == 0)
-                stalled = true;
-            gave_up |= late;
-        }
+        pipe_wait<RingWaitConst<T>::value>(&full[s], phase, pw, a.wait_polls, armer, a.err);
 
         f32x2 sv[NV][PR];
         P scp[NV], shp[NV];
@@ -176,9 +170,9 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
         }
         // the CTA barrier inside the reduction also means every thread of this
         // CTA has copied stage s out, so it can be refilled
-        float total = cluster_sum(f2_sum(ss2), red, xc, nred++, rank, cs, a.err, a.wait_polls, gave_up, stalled);
+        float total = cluster_sum<RingWaitConst<T>::value>(f2_sum(ss2), red, xc, nred++, rank, cs, a.err, a.wait_polls, armer, pw);
         if (threadIdx.x == 0 && k + nst < nrows) {
-            if (!stalled) {   // thread 0 saw stage s's phase complete: refill it
+            if (!pw.stalled) {   // thread 0 saw stage s's phase complete: refill it
                 fence_proxy_async_smem();
                 issue(k + nst, s);
             } else if (stall_rows < 0) {
@@ -201,7 +195,7 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
                     }
                 }
             }
-            total = cluster_sum(f2_sum(ss2), red, xc, nred++, rank, cs, a.err, a.wait_polls, gave_up, stalled);
+            total = cluster_sum<RingWaitConst<T>::value>(f2_sum(ss2), red, xc, nred++, rank, cs, a.err, a.wait_polls, armer, pw);
         }
         const float rrms = rsqrtf(total * ih + a.eps);
         if (rank == 0 && threadIdx.x == 0) {
@@ -246,7 +240,7 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
     }
     // Only a stalled CTA can exit with copies in flight: thread 0 gives the
     // last issued phase of every stage one more bounded wait.
-    if (stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
+    if (pw.stalled) drain_ring(full, nst, stall_rows < 0 ? nrows : stall_rows);
     // no CTA leaves while another may still address its shared memory
     cluster_sync();
 }

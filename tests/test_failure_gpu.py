@@ -94,15 +94,19 @@ def test_plain_ring_forward_flag(timeout_test_mode):
     assert rn.rmsnorm_read_device_errors() == 0
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("H", [4096, 32768])
-def test_one_poll_limit_finishes(oracle, timeout_test_mode, H):
-    """A one-poll limit with nothing held: threads whose waits run out carry
-    on with the shortened limit while each CTA's issuing thread (and, on the
-    split-row kernels, the thread that arms the cluster exchange) waits for
-    every copy and partial sum it armed.  The calls finish, whether or not
-    a wait ran out this time; normal calls afterwards match the oracle."""
+def test_one_poll_limit_finishes(oracle, timeout_test_mode, dtype, H):
+    """A one-poll limit with nothing held.  The f16 kernels take their wait
+    limit from the call: their threads whose waits run out carry on with the
+    shortened limit while each CTA's issuing thread (and, on the split-row
+    kernels, the thread that arms the cluster exchange) waits for every copy
+    and partial sum it armed.  The bf16 kernels poll against the full limit
+    until a wait has run out, so the setting leaves them as they are.  Either
+    way the calls finish, whether or not a wait ran out this time, and normal
+    calls afterwards match the oracle."""
     M = 2049 if H == 4096 else 129
-    (x, r, w, dy), (tx, tr, tw, tdy) = _inputs(M, H, seed=H)
+    (x, r, w, dy), (tx, tr, tw, tdy) = _inputs(M, H, dtype, seed=H)
     timeout_test_mode(1, False)
     for _ in range(3):
         y, s, rr = _fused(tx, tr, tw)
@@ -114,8 +118,8 @@ def test_one_poll_limit_finishes(oracle, timeout_test_mode, H):
     y, s, rr = _fused(tx, tr, tw)
     torch.cuda.synchronize()
     assert rn.rmsnorm_read_device_errors() == 0
-    ref = oracle.rmsnorm_fwd(x, w, 1e-5, "bf16", residual=r)
-    assert check_fwd_values(wl.from_torch(y, "bf16"), ref["y"], "bf16", oracle)["failed"] == 0
+    ref = oracle.rmsnorm_fwd(x, w, 1e-5, dtype, residual=r)
+    assert check_fwd_values(wl.from_torch(y, dtype), ref["y"], dtype, oracle)["failed"] == 0
 
 
 def test_debug_setting_validation():
