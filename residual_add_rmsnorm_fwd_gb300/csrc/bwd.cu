@@ -266,13 +266,19 @@ inline int reduce_slices(int G) {
     return s < 1 ? 1 : (s > kReduceSlices ? kReduceSlices : s);
 }
 
+// SFIX > 0: the slice count as a compile-time constant (the ring backward's
+// usual 32), so the final sum over the slices is unrolled -- its loads issue
+// together instead of one load-add chain (measured 0.35 us less per call);
+// SFIX = 0: S = blockDim.x / 32 at run time.  The order of the additions is
+// the same either way.
+template <int SFIX>
 __global__ void __launch_bounds__(32 * kReduceSlices)
     dweight_reduce_kernel(const float *__restrict__ partial, int G, int H, float *__restrict__ dweight) {
     // launched as a programmatic dependent of the backward: its partials are
     // complete and visible only after this wait
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float part[kReduceSlices][33];
-    const int S = (int)(blockDim.x >> 5);
+    const int S = SFIX > 0 ? SFIX : (int)(blockDim.x >> 5);
     const int col = threadIdx.x & 31, k = threadIdx.x >> 5;
     const int h = blockIdx.x * 32 + col;
     float s = 0.0f;
@@ -294,7 +300,12 @@ __global__ void __launch_bounds__(32 * kReduceSlices)
     __syncthreads();
     if (k == 0 && h < H) {
         float t = 0.0f;
-        for (int q = 0; q < S; ++q) t += part[q][col];
+        if constexpr (SFIX > 0) {
+#pragma unroll
+            for (int q = 0; q < SFIX; ++q) t += part[q][col];
+        } else {
+            for (int q = 0; q < S; ++q) t += part[q][col];
+        }
         dweight[h] = t;
     }
 }
@@ -466,7 +477,9 @@ cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, 
         cfg.numAttrs = 1;
         const float *part = a.partial;
         const int G = p.partial_rows, H = a.H;
-        e = cudaLaunchKernelEx(&cfg, dweight_reduce_kernel, part, G, H, dweight);
+        e = reduce_slices(G) == kReduceSlices
+                ? cudaLaunchKernelEx(&cfg, dweight_reduce_kernel<kReduceSlices>, part, G, H, dweight)
+                : cudaLaunchKernelEx(&cfg, dweight_reduce_kernel<0>, part, G, H, dweight);
     }
     return e;
 }

@@ -29,13 +29,14 @@ struct FwdArgs {
     int has_w;
     unsigned *err;        // device error word (bounded pipeline waits report here)
     uint32_t wait_polls;  // polls before a pipeline wait gives up (kWaitPolls unless under test)
-    int hold_first;       // test of the time-out path: each ring CTA holds back its first row
-                          // copy until its first wait has given up (0 in normal use)
+    int hold_first;       // test of the time-out path: the issuing thread of each ring CTA waits
+                          // for its first row before issuing any copy (0 in normal use)
     // AdaLN conditioning: token row i reads scale/shift row i / rows_per_cond
     const void *scale;
     const void *shift;
     int64_t cond_stride;
     int64_t rows_per_cond;   // 1..M (clamped to M by the host), so row / rows_per_cond fits 32 bits
+    int64_t cond_groups;     // shared AdaLN on the ring: conditioning rows each given their own CTAs, or 0
     // LayerNorm: bias (H,) or nullptr, and the saved per-row mean (M) or
     // nullptr; rrms then holds the per-row rstd
     const void *b;

@@ -106,6 +106,16 @@ def test_adaln_grid_stride(oracle, dtype, H, M, rpc):
     assert_ok(run_adaln(oracle, dtype, M, H, rows_per_cond=rpc, seed=M))
 
 
+@pytest.mark.parametrize("dtype,H,M,rpc", [("bf16", 2048, 12289, 6144), ("bf16", 2048, 12288, 6144),
+                                           ("f16", 4096, 20001, 1000), ("bf16", 2048, 9001, 37),
+                                           ("f32", 2048, 8191, 2000), ("bf16", 8192, 4099, 1024)])
+def test_adaln_conditioning_groups(oracle, dtype, H, M, rpc):
+    """Few conditioning rows on the bulk-copy ring: each gets its own group of
+    CTAs, sized by its rows (a ragged last row gets a small group), every
+    row of x processed once with its own conditioning row."""
+    assert_ok(run_adaln(oracle, dtype, M, H, rows_per_cond=rpc, seed=M + rpc))
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("H", [64, 2048, 4096, 8192, 32768])
 def test_adaln_broadcast_is_bitwise_repeated_rows(oracle, dtype, H):
