@@ -135,9 +135,9 @@ int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, int sms, cudaS
         return to_status(launch_fwd_warp(a, dtype, mode, sms, s));
     RingPlan ring;
     if (vec && mode == kAdaln && plan_fwd_ring(a.M, a.H, dtype, kAdalnShared, sms, &ring)) {
-        // few conditioning rows (at least four CTAs each): one group of CTAs
+        // few conditioning rows (at most one per four CTAs): one group of CTAs
         // per conditioning row, so each CTA reads a single one (bf16 12288 x
-        // 2048, two rows: 20.1 -> 19.2 us per call); else the plain stride
+        // 2048, two rows: 20.1 -> 19.4 us per call); else the plain stride
         // when a conditioning row spans four of a CTA's strides of rows
         const int64_t n_cond = (a.M - 1) / a.rows_per_cond + 1;
         if (4 * n_cond <= (int64_t)ring.grid) {

@@ -84,22 +84,24 @@ __device__ __forceinline__ void xchg_init(ClusterXchg &xc) {
 }
 
 // Sum of v over every thread of the cluster, reduction number j (0, 1, 2, ...
-// in every CTA).  The CTA's sum (block_sum over `red`, bank j mod 2) is
+// in every CTA), in two halves so that the caller can act in between (refill
+// the stage the CTA has just copied out) while the other CTAs' sums travel.
+// cluster_push: the CTA's sum (block_sum over `red`, bank j mod 2) is
 // written by one thread into its own slot and pushed into slot `rank` of
-// every other CTA with st.async; each CTA's mbarrier j mod 2 completes once
-// its own arrival and the other CTAs' bytes are in, and every thread then
-// adds the slots in rank order, so all threads of the cluster hold the
-// bit-identical total.  No CTA waits for another to arrive anywhere: each
-// waits only for the partial sums it needs.  Slots and barrier j mod 2 are
-// used again by reduction j + 2, which another CTA can start only after this
-// CTA has sent its partial of reduction j + 1, i.e. after it has read the
-// slots of reduction j.  The wait is bounded: a wait still incomplete after
-// `polls` polls records kErrPipelineTimeout in *err (pipe_wait); the arming
-// thread (thread 0) waits on up to kWaitPolls so that it never re-arms an
-// incomplete phase, and arms nothing more (stalled) if even that runs out.
-template <bool WAIT_CONST>
-__device__ __forceinline__ float cluster_sum(float v, float *red, ClusterXchg &xc, uint32_t j, uint32_t rank,
-                                             uint32_t cs, unsigned *err, uint32_t polls, bool armer, PipeWait &pw) {
+// every other CTA with st.async.  cluster_total: each CTA's mbarrier j mod 2
+// completes once its own arrival and the other CTAs' bytes are in, and every
+// thread then adds the slots in rank order, so all threads of the cluster
+// hold the bit-identical total.  No CTA waits for another to arrive
+// anywhere: each waits only for the partial sums it needs.  Slots and barrier
+// j mod 2 are used again by reduction j + 2, which another CTA can start only
+// after this CTA has sent its partial of reduction j + 1, i.e. after it has
+// read the slots of reduction j.  The wait is bounded: a wait still
+// incomplete after `polls` polls records kErrPipelineTimeout in *err
+// (pipe_wait); the arming thread (thread 0) waits on up to kWaitPolls so that
+// it never re-arms an incomplete phase, and arms nothing more (stalled) if
+// even that runs out.
+__device__ __forceinline__ void cluster_push(float v, float *red, ClusterXchg &xc, uint32_t j, uint32_t rank,
+                                             uint32_t cs, bool armer, const PipeWait &pw) {
     const int b = (int)(j & 1u);
     const float t = block_sum(v, red, b);
     if (armer) {
@@ -112,10 +114,23 @@ __device__ __forceinline__ float cluster_sum(float v, float *red, ClusterXchg &x
             }
         }
     }
+}
+
+template <bool WAIT_CONST>
+__device__ __forceinline__ float cluster_total(ClusterXchg &xc, uint32_t j, uint32_t cs, unsigned *err,
+                                               uint32_t polls, bool armer, PipeWait &pw) {
+    const int b = (int)(j & 1u);
     pipe_wait<WAIT_CONST>(&xc.bar[b], (j >> 1) & 1u, pw, polls, armer, err);
     float total = 0.0f;
     for (uint32_t q = 0; q < cs; ++q) total += xc.slot[b][q];
     return total;
+}
+
+template <bool WAIT_CONST>
+__device__ __forceinline__ float cluster_sum(float v, float *red, ClusterXchg &xc, uint32_t j, uint32_t rank,
+                                             uint32_t cs, unsigned *err, uint32_t polls, bool armer, PipeWait &pw) {
+    cluster_push(v, red, xc, j, rank, cs, armer, pw);
+    return cluster_total<WAIT_CONST>(xc, j, cs, err, polls, armer, pw);
 }
 
 }  // namespace rmsn

@@ -132,7 +132,11 @@ __global__ void __launch_bounds__(512) __maxnreg__(fwd_ring_max_regs(NV, MODE))
     // weight (H,), by column only, widened once per CTA; ones without weight.
     // With shared conditioning rows wv holds w * (1 + scale) of the current
     // conditioning row instead, and shc its shift: refreshed only when the
-    // CTA's next row belongs to another conditioning row.
+    // CTA's next row belongs to another conditioning row.  The refresh loads
+    // are issued before the row's stage wait and w * (1 + scale) is formed
+    // after it, so their latency hides behind the wait (bf16 12288 x 2048,
+    // one conditioning row: the first row of a CTA was ready about 1 us later
+    // than in the plain norm when the product was formed before the wait).
     f32x2 wv[NV][PR];
     auto load_w = [&](int i) {
         const int c = threadIdx.x + i * blockDim.x;
@@ -162,28 +166,40 @@ __global__ void __launch_bounds__(512) __maxnreg__(fwd_ring_max_regs(NV, MODE))
     for (int64_t k = 0; k < nrows; ++k) {
         const int64_t row = r0 + k * G;
         const int64_t base = row * a.stride;
-        if constexpr (MODE == kAdalnShared) {
+        if constexpr (MODE != kAdalnShared) {
+            pipe_wait<RingWaitConst<T>::value>(&full[s], phase, pw, a.wait_polls, armer, a.err);
+        } else {
             // rows of a CTA only increase: divide only when a boundary is passed
             // (the same in every thread)
             if (row >= c_next) {
+                // the new conditioning row's weight and scale, packed; every
+                // thread sets all of wv and shc (columns past the row: w = 1,
+                // scale = shift = 0, never stored), so the old ones are dead here
+                P wpk[NV], scpk[NV];
                 const uint32_t cr = (uint32_t)row / (uint32_t)a.rows_per_cond;
                 c_next = (int64_t)(cr + 1) * a.rows_per_cond;
                 const int64_t cbase = (int64_t)cr * a.cond_stride;
 #pragma unroll
                 for (int i = 0; i < NV; ++i) {
                     const int c = threadIdx.x + i * blockDim.x;
-                    if (c < nvec) {
-                        f32x2 wt[PR], sc[PR];
-                        widen16<T>(load_w(i), wt);
-                        widen16<T>(ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC), sc);
-#pragma unroll
-                        for (int q = 0; q < PR; ++q) wv[i][q] = f2_fma(wt[q], sc[q], wt[q]);   // w * (1 + scale)
-                        shc[i] = ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC);
-                    }
+                    const bool in = c < nvec;
+                    wpk[i] = load_w(i);
+                    scpk[i] = in ? ld_cached<T, VEC>(scale + cbase + (int64_t)c * VEC) : fill<T, VEC>(from_f32<T>(0.0f));
+                    shc[i] = in ? ld_cached<T, VEC>(shift + cbase + (int64_t)c * VEC) : fill<T, VEC>(from_f32<T>(0.0f));
                 }
+                pipe_wait<RingWaitConst<T>::value>(&full[s], phase, pw, a.wait_polls, armer, a.err);
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                    f32x2 wt[PR], sc[PR];
+                    widen16<T>(wpk[i], wt);
+                    widen16<T>(scpk[i], sc);
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) wv[i][q] = f2_fma(wt[q], sc[q], wt[q]);   // w * (1 + scale)
+                }
+            } else {
+                pipe_wait<RingWaitConst<T>::value>(&full[s], phase, pw, a.wait_polls, armer, a.err);
             }
         }
-        pipe_wait<RingWaitConst<T>::value>(&full[s], phase, pw, a.wait_polls, armer, a.err);
 
         // s = x (+ residual) in binary32, kept in registers for the scale step;
         // the post-add sum is written back as the next residual stream

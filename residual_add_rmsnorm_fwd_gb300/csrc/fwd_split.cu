@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
     constexpr int VEC = Vec16<T>::n;
     constexpr int PR = Pairs16<T>::n;
     constexpr int NS = STAGE_COND ? 3 : (RESID ? 2 : 1);  // segments staged per ring slot
+    constexpr bool EARLY_REFILL = sizeof(T) == 2 && MODE == kPlain;   // stage refill before the exchange wait
     using P = Pack<T, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[64];
@@ -169,14 +170,31 @@ __global__ void __launch_bounds__(512) fwd_split_kernel(FwdArgs a, SplitShape sh
             }
         }
         // the CTA barrier inside the reduction also means every thread of this
-        // CTA has copied stage s out, so it can be refilled
-        float total = cluster_sum<RingWaitConst<T>::value>(f2_sum(ss2), red, xc, nred++, rank, cs, a.err, a.wait_polls, armer, pw);
-        if (threadIdx.x == 0 && k + nst < nrows) {
-            if (!pw.stalled) {   // thread 0 saw stage s's phase complete: refill it
-                fence_proxy_async_smem();
-                issue(k + nst, s);
-            } else if (stall_rows < 0) {
-                stall_rows = k + nst;   // rows issued before thread 0 stalled
+        // CTA has copied stage s out, so it can be refilled: before the other
+        // CTAs' partial sums are waited for in the 2-byte plain norm, whose one
+        // staged stream leaves the ring short of bytes in flight (bf16 H =
+        // 32768-131072: 5-7% faster), after it elsewhere (fused bf16 H =
+        // 32768 / 65536 and fp32: 2-7% slower refilled early)
+        cluster_push(f2_sum(ss2), red, xc, nred, rank, cs, armer, pw);
+        if constexpr (EARLY_REFILL) {
+            if (threadIdx.x == 0 && k + nst < nrows) {
+                if (!pw.stalled) {   // thread 0 saw stage s's phase complete: refill it
+                    fence_proxy_async_smem();
+                    issue(k + nst, s);
+                } else if (stall_rows < 0) {
+                    stall_rows = k + nst;   // rows issued before thread 0 stalled
+                }
+            }
+        }
+        float total = cluster_total<RingWaitConst<T>::value>(xc, nred++, cs, a.err, a.wait_polls, armer, pw);
+        if constexpr (!EARLY_REFILL) {
+            if (threadIdx.x == 0 && k + nst < nrows) {
+                if (!pw.stalled) {
+                    fence_proxy_async_smem();
+                    issue(k + nst, s);
+                } else if (stall_rows < 0) {
+                    stall_rows = k + nst;
+                }
             }
         }
         float mu = 0.0f;
