@@ -3,6 +3,7 @@
 // and launch.
 #include <cmath>
 #include <cstring>
+#include <initializer_list>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -110,6 +111,17 @@ int check_shape(int64_t M, int64_t H, int64_t stride, int dtype) {
     return RMSN_OK;
 }
 
+// The row matrices of a call (x, residual, outputs; nullptr = absent) start
+// at one offset modulo 16 bytes: with their shared row stride, every row
+// then has one alignment phase in all of them.
+bool same_phase(std::initializer_list<const void *> ps) {
+    const void *first = *ps.begin();
+    for (const void *p : ps)
+        if (p != nullptr && reinterpret_cast<uintptr_t>(p) % 16 != reinterpret_cast<uintptr_t>(first) % 16)
+            return false;
+    return true;
+}
+
 bool rows_vectorisable(int64_t H, int64_t stride, int dtype) {
     const int es = elem_bytes(dtype);
     return (H * es) % 16 == 0 && (stride * es) % 16 == 0;
@@ -123,8 +135,11 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA
 // conditioning rows each serve 1024 rows or more), the bulk-copy ring for
 // aligned rows of 4 KB (one input stream) or 8 KB and more up to 32 KB, the
 // register kernel, a cluster of CTAs per aligned row of 32-256 KB, and the
-// two-pass chunked kernel for the rest (longer or misaligned rows).
-int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, int sms, cudaStream_t s) {
+// two-pass chunked kernel for the rest (longer or misaligned rows).  Rows
+// that are not 16-byte aligned but whose matrices share one alignment phase
+// (`phased`) take the register kernel in each row's aligned frame while the
+// row fits it.
+int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, bool phased, int sms, cudaStream_t s) {
     if (a.H < kSmallH && (mode == kPlain || mode == kResid)) return to_status(launch_fwd_small(a, dtype, vec, sms, s));
     // AdaLN conditioning rows count as shared when each serves at least four
     // of a CTA's strides of rows, so a CTA rarely moves to a new one (below
@@ -150,6 +165,7 @@ int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, int sms, cudaS
     }
     if (vec && plan_fwd_ring(a.M, a.H, dtype, mode, sms, &ring))
         return to_status(launch_fwd_ring(a, dtype, mode, ring, s));
+    if (!vec && phased && fwd_phase_fits(a.H, dtype)) return to_status(launch_fwd_phase(a, dtype, mode, sms, s));
     if (fwd_row_fits(a.H, dtype, vec)) return to_status(launch_fwd_row(a, dtype, mode, vec, sms, s));
     // aligned rows above 32 KB: a cluster of CTAs per row (the same
     // shared-conditioning rule, with the cluster count as the row stride)
@@ -204,6 +220,7 @@ int forward(const void *x, const void *residual, const void *weight, void *y, vo
     bool vec = rows_vectorisable(H, row_stride, dtype);
     for (const void *p : {x, residual, w, static_cast<const void *>(y), static_cast<const void *>(residual_out)})
         if (p != nullptr && !aligned(p, 16)) vec = false;
+    const bool phased = same_phase({x, fused ? residual : nullptr, y, fused ? residual_out : nullptr});
 
     FwdArgs a{};
     a.err = device_error_word(dev);
@@ -220,7 +237,7 @@ int forward(const void *x, const void *residual, const void *weight, void *y, vo
     a.H = (int)H;
     a.eps = eps;
     a.has_w = has_weight ? 1 : 0;
-    return dispatch_fwd(a, dtype, fused ? kResid : kPlain, vec, sms, static_cast<cudaStream_t>(stream));
+    return dispatch_fwd(a, dtype, fused ? kResid : kPlain, vec, phased, sms, static_cast<cudaStream_t>(stream));
 }
 
 // AdaLN forward: rows use conditioning row i / rows_per_cond of scale and
@@ -264,6 +281,7 @@ int adaln_forward(const void *x, const void *weight, const void *scale, const vo
     bool vec = rows_vectorisable(H, row_stride, dtype) && (cond_stride * es) % 16 == 0;
     for (const void *p : {x, w, scale, shift, static_cast<const void *>(y)})
         if (p != nullptr && !aligned(p, 16)) vec = false;
+    const bool phased = same_phase({x, y});
 
     FwdArgs a{};
     a.err = device_error_word(dev);
@@ -282,7 +300,7 @@ int adaln_forward(const void *x, const void *weight, const void *scale, const vo
     a.shift = shift;
     a.cond_stride = cond_stride;
     a.rows_per_cond = rows_per_cond < M ? rows_per_cond : M;   // below 2^31, like M: 32-bit division
-    return dispatch_fwd(a, dtype, kAdaln, vec, sms, static_cast<cudaStream_t>(stream));
+    return dispatch_fwd(a, dtype, kAdaln, vec, phased, sms, static_cast<cudaStream_t>(stream));
 }
 
 // Residual + LayerNorm forward: validation as for the RMSNorm forward, plus
@@ -332,6 +350,7 @@ int layernorm_forward(const void *x, const void *residual, const void *weight, c
     bool vec = rows_vectorisable(H, row_stride, dtype);
     for (const void *p : {x, r, w, b, static_cast<const void *>(y), static_cast<const void *>(so)})
         if (p != nullptr && !aligned(p, 16)) vec = false;
+    const bool phased = same_phase({x, r, y, so});
 
     FwdArgs a{};
     a.err = device_error_word(dev);
@@ -350,7 +369,7 @@ int layernorm_forward(const void *x, const void *residual, const void *weight, c
     a.H = (int)H;
     a.eps = eps;
     a.has_w = has_weight ? 1 : 0;
-    return dispatch_fwd(a, dtype, fused ? kLnResid : kLn, vec, sms, static_cast<cudaStream_t>(stream));
+    return dispatch_fwd(a, dtype, fused ? kLnResid : kLn, vec, phased, sms, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -641,7 +660,8 @@ int backward(const void *dy, const void *dres, const void *x, const void *weight
     bool vec = rows_vectorisable(H, row_stride, dtype);
     for (const void *p : {dy, dr, x, w, static_cast<const void *>(dx)})
         if (p != nullptr && !aligned(p, 16)) vec = false;
-    const BwdPlan plan = plan_bwd(M, (int)H, dtype, vec, fused, sms);
+    const bool phased = same_phase({x, dy, dr, dx});
+    const BwdPlan plan = plan_bwd(M, (int)H, dtype, vec, phased, fused, sms);
     const size_t part_bytes = dw != nullptr ? bwd_partial_bytes(plan, (int)H) : 0;
     if (dw != nullptr) {
         if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < part_bytes)
@@ -740,10 +760,11 @@ RMSN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype, size_t
     if (st) return st;
     // the largest of the variants rmsnorm_bwd and rmsnorm_bwd_residual may pick
     size_t need = 0;
-    for (int vec = 0; vec < 2; ++vec) {
+    for (int layout = 0; layout < 3; ++layout) {   // 16-byte aligned rows, rows at one phase, other rows
+        const bool vec = layout == 0, phased = layout == 1;
         if (vec && (H * elem_bytes(dtype)) % 16 != 0) continue;
         for (int dres = 0; dres < 2; ++dres) {
-            const size_t v = bwd_partial_bytes(plan_bwd(M, (int)H, dtype, vec != 0, dres != 0, sms), (int)H);
+            const size_t v = bwd_partial_bytes(plan_bwd(M, (int)H, dtype, vec, phased, dres != 0, sms), (int)H);
             need = v > need ? v : need;
         }
     }

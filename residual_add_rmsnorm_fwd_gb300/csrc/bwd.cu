@@ -373,6 +373,7 @@ const void *kernel_for_dt(const BwdPlan &p, bool vec) {
 
 const void *kernel_for(const BwdPlan &p, int dtype, bool vec) {
     if (p.kind == kBwdRing) return bwd_ring_kernel_for(dtype, p.nv, p.dres);
+    if (p.kind == kBwdPhase) return bwd_phase_kernel_for(dtype, p.nv, p.dres);
     if (p.kind == kBwdSplit) return bwd_split_kernel_for(dtype, p.nv, p.dres);
     switch (dtype) {
     case kF32: return kernel_for_dt<float>(p, vec);
@@ -384,7 +385,7 @@ const void *kernel_for(const BwdPlan &p, int dtype, bool vec) {
 
 }  // namespace
 
-BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool dres, int sm_count) {
+BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool phased, bool dres, int sm_count) {
     BwdPlan p{};
     p.dres = dres;
     p.cs = 1;
@@ -407,6 +408,8 @@ BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool dres, int sm_count)
         p.grid = sp.grid;
         p.partial_rows = sp.grid / sp.cs;
         return p;
+    } else if (!vec && phased && bwd_phase_pick(H, dtype, &p.threads, &p.nv)) {
+        p.kind = kBwdPhase;   // misaligned rows at one phase: 128-bit accesses in the row's frame
     } else {
         const int nvec = vec ? H / vec_elems(dtype) : H;
         p.kind = pick_row(nvec, vec, p.threads, p.nv) ? kBwdRow : kBwdChunked;

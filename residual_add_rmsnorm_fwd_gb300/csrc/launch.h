@@ -90,6 +90,12 @@ cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, int mode, int sm_count,
 bool fwd_row_fits(int H, int dtype, bool vec);
 cudaError_t launch_fwd_row(const FwdArgs &a, int dtype, int mode, bool vec, int sm_count, cudaStream_t st);
 
+// Rows that are not 16-byte aligned, with x, the residual and the outputs at
+// one alignment phase: the register-row kernel in each row's aligned frame
+// (128-bit accesses, masked first and last vectors).
+bool fwd_phase_fits(int H, int dtype);
+cudaError_t launch_fwd_phase(const FwdArgs &a, int dtype, int mode, int sm_count, cudaStream_t st);
+
 // Aligned rows above 32 KB: a cluster of CTAs per row, one segment each.
 bool plan_fwd_split(int64_t M, int H, int dtype, int mode, int sm_count, SplitPlan *out);
 cudaError_t launch_fwd_split(const FwdArgs &a, int dtype, int mode, const SplitPlan &p, cudaStream_t st);
@@ -99,7 +105,7 @@ cudaError_t launch_fwd_chunked(const FwdArgs &a, int dtype, int mode, bool vec, 
 
 // Backward: dx per row plus per-CTA dweight partials, then the fixed-order
 // column reduction of the partials.
-enum BwdKind { kBwdRow = 0, kBwdChunked = 1, kBwdRing = 2, kBwdSplit = 3 };
+enum BwdKind { kBwdRow = 0, kBwdChunked = 1, kBwdRing = 2, kBwdSplit = 3, kBwdPhase = 4 };
 struct BwdPlan {
     int kind;          // BwdKind
     bool dres;         // adds the residual stream's gradient (fused-forward backward)
@@ -114,7 +120,12 @@ struct BwdPlan {
 };
 const void *bwd_ring_kernel_for(int dtype, int nv, bool dres);
 const void *bwd_split_kernel_for(int dtype, int nv, bool dres);
-BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool dres, int sm_count);
+// Rows that are not 16-byte aligned, with dy, x, dx (and dresidual_out) at one
+// alignment phase: the register-row backward in each row's aligned frame.
+bool bwd_phase_pick(int H, int dtype, int *threads, int *nv);
+const void *bwd_phase_kernel_for(int dtype, int nv, bool dres);
+// `phased`: the rows are not 16-byte aligned but share one phase (above).
+BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool phased, bool dres, int sm_count);
 size_t bwd_partial_bytes(const BwdPlan &p, int H);
 cudaError_t launch_bwd(const BwdArgs &a, const BwdPlan &p, int dtype, bool vec, float *dweight,
                        cudaStream_t st);

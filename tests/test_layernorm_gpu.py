@@ -32,8 +32,10 @@ def rows_for(H, cap=300_000):
 
 
 def run_ln(oracle, dtype, M, H, residual=False, weight=True, bias=True, stride=None, offset=0, eps=1e-5, seed=0,
-           in_place=False, x_np=None, r_np=None, w_np=None, b_np=None, shift=0.0):
+           in_place=False, x_np=None, r_np=None, w_np=None, b_np=None, shift=0.0, w_offset=None):
+    """w_offset: the weight's and bias's own element offset (default: offset)."""
     stride = H if stride is None else stride
+    w_offset = offset if w_offset is None else w_offset
     rng = wl.rng_for(seed)
     if x_np is None:
         x = wl.matrix(rng, M, H, dtype, stride)
@@ -48,8 +50,8 @@ def run_ln(oracle, dtype, M, H, residual=False, weight=True, bias=True, stride=N
     gr = Guarded(M, H, stride, dtype, offset).upload(r) if residual else None
     gy = gx if in_place else Guarded(M, H, stride, dtype, offset)
     gs = (gr if in_place else Guarded(M, H, stride, dtype, offset)) if residual else None
-    wd = device_vec(w, dtype, offset) if weight else None
-    bd = device_vec(b, dtype, offset) if bias else None
+    wd = device_vec(w, dtype, w_offset) if weight else None
+    bd = device_vec(b, dtype, w_offset) if bias else None
     mean = f32_buffer(M, offset)
     rstd = f32_buffer(M, offset)
     if residual:

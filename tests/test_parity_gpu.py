@@ -39,8 +39,10 @@ def rows_for(H, cap=400_000):
 
 
 def run_fwd(oracle, dtype, M, H, stride=None, residual=False, weight=True, save_rrms=True, offset=0,
-            eps=1e-5, seed=0, x_np=None, r_np=None, w_np=None):
+            eps=1e-5, seed=0, x_np=None, r_np=None, w_np=None, w_offset=None):
+    """w_offset: the weight's own element offset (default: offset)."""
     stride = H if stride is None else stride
+    w_offset = offset if w_offset is None else w_offset
     rng = wl.rng_for(seed)
     x = wl.matrix(rng, M, H, dtype, stride) if x_np is None else x_np
     r = (wl.matrix(rng, M, H, dtype, stride) if r_np is None else r_np) if residual else None
@@ -49,7 +51,7 @@ def run_fwd(oracle, dtype, M, H, stride=None, residual=False, weight=True, save_
     gy = Guarded(M, H, stride, dtype, offset)
     gr = Guarded(M, H, stride, dtype, offset).upload(r) if residual else None
     gs = Guarded(M, H, stride, dtype, offset) if residual else None
-    wd = device_vec(w, dtype, offset) if weight else None
+    wd = device_vec(w, dtype, w_offset) if weight else None
     rrms = f32_buffer(M, offset) if save_rrms else None
     if residual:
         rn.rmsnorm_fwd_residual(gx.t, gr.t, wd, gy.t, gs.t, rrms, eps=eps)
@@ -179,11 +181,12 @@ def test_zero_rows_no_launch():
 # ---------------------------------------------------------------- backward --
 
 def run_bwd(oracle, dtype, M, H, stride=None, weight=True, offset=0, eps=1e-5, seed=0, want_dw=True,
-            fused=False):
+            fused=False, w_offset=None):
     stride = H if stride is None else stride
+    w_offset = offset if w_offset is None else w_offset
     rng = wl.rng_for(seed)
     fwd = run_fwd(oracle, dtype, M, H, stride=stride, residual=fused, weight=weight, offset=offset,
-                  eps=eps, seed=seed)
+                  eps=eps, seed=seed, w_offset=w_offset)
     assert_fwd_ok(fwd)
     # the input the backward sees: x, or residual_out for the fused forward
     xin = fwd["gs"] if fused else None
@@ -196,7 +199,7 @@ def run_bwd(oracle, dtype, M, H, stride=None, weight=True, offset=0, eps=1e-5, s
         gx = Guarded(M, H, stride, dtype, offset).upload(fwd["x"])
     gdx = Guarded(M, H, stride, dtype, offset)
     w = fwd["w"]
-    wd = device_vec(w, dtype, offset) if weight else None
+    wd = device_vec(w, dtype, w_offset) if weight else None
     dw = f32_buffer(H) if (weight and want_dw) else None
     nbytes = rn.rmsnorm_bwd_workspace_bytes(M, H, dtype=wl.torch_dtype(dtype))
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda") if dw is not None else None
@@ -212,12 +215,13 @@ def run_bwd(oracle, dtype, M, H, stride=None, weight=True, offset=0, eps=1e-5, s
     return out
 
 
-def run_bwd_residual(oracle, dtype, M, H, stride=None, weight=True, offset=0, eps=1e-5, seed=0):
+def run_bwd_residual(oracle, dtype, M, H, stride=None, weight=True, offset=0, eps=1e-5, seed=0, w_offset=None):
     """Fused forward, then the fused backward with an incoming residual-stream gradient."""
     stride = H if stride is None else stride
+    w_offset = offset if w_offset is None else w_offset
     rng = wl.rng_for(seed + 1000)
     fwd = run_fwd(oracle, dtype, M, H, stride=stride, residual=True, weight=weight, offset=offset, eps=eps,
-                  seed=seed)
+                  seed=seed, w_offset=w_offset)
     assert_fwd_ok(fwd)
     s_np = fwd["gs"].host()
     dy = wl.matrix(rng, M, H, dtype, stride)
@@ -226,7 +230,7 @@ def run_bwd_residual(oracle, dtype, M, H, stride=None, weight=True, offset=0, ep
     gdr = Guarded(M, H, stride, dtype, offset).upload(dres)
     gdx = Guarded(M, H, stride, dtype, offset)
     w = fwd["w"]
-    wd = device_vec(w, dtype, offset) if weight else None
+    wd = device_vec(w, dtype, w_offset) if weight else None
     dw = f32_buffer(H) if weight else None
     nbytes = rn.rmsnorm_bwd_workspace_bytes(M, H, wl.torch_dtype(dtype))
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda") if dw is not None else None
