@@ -4,7 +4,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                     [--workload step|fused_fwd|fused_fwd_bwd_residual|dit_mix|fwd_f32_small|
                                 fwd_bwd_8192|fused_f16_padded|adaln|adaln_per_token|
-                                ln_residual|ln_residual_f32|ln_plain|long_rows]
+                                ln_residual|ln_residual_f32|ln_plain|long_rows|odd_rows]
 
 Default workload ("step"): one pass of the whole hot path on the
 (B=8, T=2048, H=4096) bf16 activations, M = 16384 rows -- the fused
@@ -602,6 +602,7 @@ WORKLOADS = {
     "fwd_bwd_8192": lambda: StepWorkload(4, backward=True),
     "fused_f16_padded": lambda: StepWorkload(5, backward=True),
     "long_rows": lambda: StepWorkload(6, backward=True),
+    "odd_rows": lambda: StepWorkload(7, backward=True),
 }
 
 

@@ -165,7 +165,11 @@ int dispatch_fwd(const FwdArgs &a, int dtype, int mode, bool vec, bool phased, i
     }
     if (vec && plan_fwd_ring(a.M, a.H, dtype, mode, sms, &ring))
         return to_status(launch_fwd_ring(a, dtype, mode, ring, s));
-    if (!vec && phased && fwd_phase_fits(a.H, dtype)) return to_status(launch_fwd_phase(a, dtype, mode, sms, s));
+    if (!vec && phased) {
+        if (plan_fwd_ring_phase(a.M, a.H, dtype, mode, sms, &ring))
+            return to_status(launch_fwd_ring_phase(a, dtype, mode, ring, s));
+        if (fwd_phase_fits(a.H, dtype)) return to_status(launch_fwd_phase(a, dtype, mode, sms, s));
+    }
     if (fwd_row_fits(a.H, dtype, vec)) return to_status(launch_fwd_row(a, dtype, mode, vec, sms, s));
     // aligned rows above 32 KB: a cluster of CTAs per row (the same
     // shared-conditioning rule, with the cluster count as the row stride)

@@ -374,6 +374,7 @@ const void *kernel_for_dt(const BwdPlan &p, bool vec) {
 const void *kernel_for(const BwdPlan &p, int dtype, bool vec) {
     if (p.kind == kBwdRing) return bwd_ring_kernel_for(dtype, p.nv, p.dres);
     if (p.kind == kBwdPhase) return bwd_phase_kernel_for(dtype, p.nv, p.dres);
+    if (p.kind == kBwdRingPhase) return bwd_ring_phase_kernel_for(dtype, p.nv, p.dres);
     if (p.kind == kBwdSplit) return bwd_split_kernel_for(dtype, p.nv, p.dres);
     switch (dtype) {
     case kF32: return kernel_for_dt<float>(p, vec);
@@ -408,6 +409,12 @@ BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool phased, bool dres, 
         p.grid = sp.grid;
         p.partial_rows = sp.grid / sp.cs;
         return p;
+    } else if (!vec && phased && bwd_ring_phase_geometry(H, dtype, dres, &rp)) {
+        p.kind = kBwdRingPhase;   // misaligned rows at one phase of 2-32 KB: the ring in the row's frame
+        p.threads = rp.threads;
+        p.nv = rp.nv;
+        p.smem_bytes = rp.smem_bytes;
+        p.ring = rp.shape;
     } else if (!vec && phased && bwd_phase_pick(H, dtype, &p.threads, &p.nv)) {
         p.kind = kBwdPhase;   // misaligned rows at one phase: 128-bit accesses in the row's frame
     } else {
@@ -424,7 +431,12 @@ BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool phased, bool dres, 
     if (p.kind == kBwdChunked && vec && (size_t)H * 4 <= kChunkedSmemAccBytes) smem_occ = (size_t)H * 4;
     if (k != nullptr && allow_dynamic_smem(k, smem_occ) == cudaSuccess)
         occ = occupancy(k, p.threads, smem_occ);
-    const int64_t cap = (int64_t)(occ > 0 ? occ : 1) * sm_count;
+    int64_t cap = (int64_t)(occ > 0 ? occ : 1) * sm_count;
+    // rows not 16-byte aligned: a grid that is a multiple of V (elements per
+    // 16 bytes) gives every row of a CTA the same phase, which the kernels'
+    // dweight registers need (rows G apart are a multiple of 16 bytes apart)
+    const int V = vec_elems(dtype);
+    if ((p.kind == kBwdPhase || p.kind == kBwdRingPhase) && M > cap && cap >= V) cap = cap / V * V;
     p.grid = (int)(M < cap ? (M > 0 ? M : 1) : cap);
     p.partial_rows = p.grid;
     return p;

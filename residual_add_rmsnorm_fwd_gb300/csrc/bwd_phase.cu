@@ -5,15 +5,12 @@
 // dx and the per-row dot product are computed in each row's aligned frame
 // with 128-bit accesses (phase.cuh), as the register-row backward does for
 // aligned rows ("Skill: Write a Triton RMSNorm Kernel", Required reasoning
-// 12).  The dweight partials need a thread-to-column map that does not move
-// from row to row, so they are kept in the column frame instead: a thread
-// owns the columns m*V ... m*V + V - 1 of its frame vectors m.  A frame
-// vector of a row at phase p holds the last V - p of those columns in its
-// elements p ... V - 1 and the first p of them sit in the next frame vector,
-// which the next lane holds: the thread takes them with p warp shuffles (the
-// last lane of a warp from the next warp's first lane, through shared memory
-// behind the row's reduction barrier).  Each column is summed over the CTA's
-// rows in row order, so dweight stays bit-reproducible.
+// 12).  The dweight terms stay in registers across a CTA's rows, which needs
+// every row of a CTA to put the same columns in the same frame vectors: the
+// host makes the grid G a multiple of V whenever a CTA has more than one row,
+// so the CTA's rows, G * stride elements apart, all have the CTA's phase.
+// Each column is summed over the CTA's rows in row order, so dweight stays
+// bit-reproducible.
 #include "launch.h"
 #include "phase.cuh"
 
@@ -25,9 +22,6 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(BwdArgs a) {
     constexpr int PR = V / 2;
     using P = Pack<T, V>;
     __shared__ float red[64];
-    // first lane of every warp: its dweight terms, for the previous warp's
-    // last lane (two banks, alternated per row like `red`)
-    __shared__ float edge[2][16][NV][V];
     // dx may be dy, x or dres itself (in-place calls): not restrict
     const T *dy = static_cast<const T *>(a.dy);
     const T *dres = static_cast<const T *>(a.dres);
@@ -38,14 +32,17 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(BwdArgs a) {
     const float ih = 1.0f / (float)H;   // one division per CTA; exact for power-of-two H
     const int qw = a.has_w ? elem_phase(w) : 0;
     const int k0 = threadIdx.x, kstep = blockDim.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const bool want_dw = a.partial != nullptr;
 
-    float acc[NV][V];   // dweight terms of columns m*V + j, m = k0 + i * kstep
+    // dweight terms of this thread's frame vectors k = k0 + i * kstep, element
+    // j: column k*V + j - pc, pc the phase of every row of this CTA (the host
+    // makes the grid a multiple of V whenever a CTA has more than one row, so
+    // rows G apart are G * stride elements apart, a multiple of 16 bytes)
+    const int pc = elem_phase(x + (int64_t)blockIdx.x * a.stride);
+    f32x2 acc[NV][PR];
 #pragma unroll
     for (int i = 0; i < NV; ++i)
 #pragma unroll
-        for (int j = 0; j < V; ++j) acc[i][j] = 0.0f;
+        for (int q = 0; q < PR; ++q) acc[i][q] = f2_make(0.0f, 0.0f);
 
     P wp[NV];
     int p_w = -1;
@@ -57,7 +54,7 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(BwdArgs a) {
         const float rr = __ldg(a.rrms + row);
         const f32x2 rr2 = f2_make(rr, rr);
         if (p != p_w) {
-            if (a.has_w) ld_op_windows<T, NV>(w, qw, p, H, k0, kstep, nf, from_f32<T>(0.0f), wp);
+            if (a.has_w) ld_op_windows<T, NV>(w, qw, p, H, k0, kstep, nf, false, wp);
             else
 #pragma unroll
                 for (int i = 0; i < NV; ++i) wp[i] = fill<T, V>(one<T>());
@@ -77,30 +74,13 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(BwdArgs a) {
                 widen16<T>(xp[i], xv);
                 widen16<T>(wp[i], wv);
 #pragma unroll
-                for (int q = 0; q < PR; ++q) dot2 = f2_fma(f2_mul(d[q], wv[q]), f2_mul(xv[q], rr2), dot2);
-            } else {   // past the row: zeros, so the dweight terms below are zero
-                gp[i] = fill<T, V>(from_f32<T>(0.0f));
-                xp[i] = gp[i];
+                for (int q = 0; q < PR; ++q) {
+                    const f32x2 xh = f2_mul(xv[q], rr2);
+                    dot2 = f2_fma(f2_mul(d[q], wv[q]), xh, dot2);
+                    acc[i][q] = f2_fma(d[q], xh, acc[i][q]);   // dweight terms (zero outside the row)
+                }
             }
         }
-        // dweight terms dy * xhat of frame vector i (zero outside the row)
-        auto terms = [&](int i, float (&t)[V]) {
-            f32x2 d[PR], xv[PR];
-            widen16<T>(gp[i], d);
-            widen16<T>(xp[i], xv);
-#pragma unroll
-            for (int q = 0; q < PR; ++q) f2_split(f2_mul(d[q], f2_mul(xv[q], rr2)), t[2 * q], t[2 * q + 1]);
-        };
-        if (want_dw && lane == 0) {   // thread 0's vector i is also thread T-1's next vector for i - 1
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                float t[V];
-                terms(i, t);
-#pragma unroll
-                for (int j = 0; j < V; ++j) edge[bank][warp][i][j] = t[j];
-            }
-        }
-        // the reduction barrier also publishes `edge`
         const float c_row = block_sum(f2_sum(dot2), red, bank) * ih;
 
         // dx = rrms * (g - xhat * c) (+ dres), as the ring backward evaluates it
@@ -129,47 +109,10 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(BwdArgs a) {
             }
         }
 
-        // dweight: column m*V + j is element j + p of frame vector m (j < V - p)
-        // or element j + p - V of frame vector m + 1, held by the next lane
-        // (the next warp's first lane for the last lane, thread 0's next
-        // vector for the CTA's last thread)
-        if (want_dw) {
-            with_shift<T>(p, [&](auto Pc) {
-                constexpr int PP = decltype(Pc)::value;
-#pragma unroll
-                for (int i = 0; i < NV; ++i) {
-                    float tw[V];
-                    terms(i, tw);
-                    float nx[PP + 1];   // elements 0 .. PP-1 of frame vector m + 1
-#pragma unroll
-                    for (int j = 0; j < PP; ++j) nx[j] = __shfl_down_sync(0xffffffffu, tw[j], 1);
-                    if (lane == 31) {
-                        const bool last = warp == nwarps - 1;
-#pragma unroll
-                        for (int j = 0; j < PP; ++j)
-                            nx[j] = last ? (i + 1 < NV ? edge[bank][0][i + 1 < NV ? i + 1 : 0][j] : 0.0f)
-                                         : edge[bank][warp + 1][i][j];
-                    }
-#pragma unroll
-                    for (int j = 0; j < V; ++j) acc[i][j] += j < V - PP ? tw[j + PP] : nx[j + PP - V];
-                }
-            });
-        }
         bank ^= 1;
     }
 
-    if (want_dw) {
-        float *prow = a.partial + (int64_t)blockIdx.x * H;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int m = k0 + i * kstep;
-#pragma unroll
-            for (int j = 0; j < V; ++j) {
-                const int c = m * V + j;
-                if (c < H) prow[c] = acc[i][j];
-            }
-        }
-    }
+    if (a.partial != nullptr) store_partial<T, NV, false>(a.partial + (int64_t)blockIdx.x * H, acc, pc, H, k0, kstep);
     allow_dependent_launch();
 }
 
@@ -186,7 +129,7 @@ inline int frame_vectors(int H, int dtype) {
     return (H + 2 * V - 2) / V;
 }
 
-// At most 512 threads (16 warps: the size of `edge`), 1..4 frame vectors each.
+// At most 512 threads, 1..4 frame vectors each.
 bool pick(int nf, int &threads, int &nv) {
     for (int k : kNV) {
         const int t = round_up((nf + k - 1) / k, 32);

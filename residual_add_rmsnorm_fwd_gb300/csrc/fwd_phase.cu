@@ -102,18 +102,19 @@ __global__ void __launch_bounds__(512) fwd_phase_kernel(FwdArgs a) {
                     f32x2 sv[PR];
                     s_pairs(i, sv);
                     const int c0 = k * V - p;
-                    const bool whole = c0 >= 0 && c0 + V <= H;
 #pragma unroll
-                    for (int q = 0; q < PR; ++q) {
-                        f32x2 d = f2_add(sv[q], nm2);
-                        if (!whole) {   // columns outside the row add nothing
+                    for (int q = 0; q < PR; ++q) sv[q] = f2_add(sv[q], nm2);
+                    if (c0 < 0 || c0 + V > H) {   // columns outside the row add nothing
+#pragma unroll
+                        for (int q = 0; q < PR; ++q) {
                             float d0, d1;
-                            f2_split(d, d0, d1);
+                            f2_split(sv[q], d0, d1);
                             const int c = c0 + 2 * q;
-                            d = f2_make(c >= 0 && c < H ? d0 : 0.0f, c + 1 >= 0 && c + 1 < H ? d1 : 0.0f);
+                            sv[q] = f2_make(c >= 0 && c < H ? d0 : 0.0f, c + 1 >= 0 && c + 1 < H ? d1 : 0.0f);
                         }
-                        ss2 = f2_fma(d, d, ss2);
                     }
+#pragma unroll
+                    for (int q = 0; q < PR; ++q) ss2 = f2_fma(sv[q], sv[q], ss2);
                 }
             }
             total = block_sum(f2_sum(ss2), red, bank);
@@ -128,12 +129,12 @@ __global__ void __launch_bounds__(512) fwd_phase_kernel(FwdArgs a) {
                 if (a.mean != nullptr) a.mean[row] = mu;
         }
         if (p != p_w) {
-            if (a.has_w) ld_op_windows<T, NV>(w, qw, p, H, k0, kstep, nf, from_f32<T>(0.0f), wp);
+            if (a.has_w) ld_op_windows<T, NV>(w, qw, p, H, k0, kstep, nf, false, wp);
             else
 #pragma unroll
                 for (int i = 0; i < NV; ++i) wp[i] = fill<T, V>(one<T>());
             if constexpr (LN) {
-                if (bias != nullptr) ld_op_windows<T, NV>(bias, qb, p, H, k0, kstep, nf, from_f32<T>(0.0f), bp);
+                if (bias != nullptr) ld_op_windows<T, NV>(bias, qb, p, H, k0, kstep, nf, false, bp);
                 else
 #pragma unroll
                     for (int i = 0; i < NV; ++i) bp[i] = fill<T, V>(from_f32<T>(0.0f));
@@ -143,10 +144,8 @@ __global__ void __launch_bounds__(512) fwd_phase_kernel(FwdArgs a) {
         P scp[NV], shp[NV];
         if constexpr (ADALN) {   // this row's conditioning row (its own phase)
             const int64_t cbase = (int64_t)((uint32_t)row / (uint32_t)a.rows_per_cond) * a.cond_stride;
-            ld_op_windows<T, NV>(scale + cbase, elem_phase(scale + cbase), p, H, k0, kstep, nf,
-                                 from_f32<T>(0.0f), scp);
-            ld_op_windows<T, NV>(shift + cbase, elem_phase(shift + cbase), p, H, k0, kstep, nf,
-                                 from_f32<T>(0.0f), shp);
+            ld_op_windows<T, NV>(scale + cbase, elem_phase(scale + cbase), p, H, k0, kstep, nf, false, scp);
+            ld_op_windows<T, NV>(shift + cbase, elem_phase(shift + cbase), p, H, k0, kstep, nf, false, shp);
         }
         const f32x2 rr2 = f2_make(rrms, rrms);
         // y = (s * rrms) * w [LayerNorm: ((s - mean) * rstd) * w + b; AdaLN:

@@ -95,6 +95,10 @@ cudaError_t launch_fwd_row(const FwdArgs &a, int dtype, int mode, bool vec, int 
 // (128-bit accesses, masked first and last vectors).
 bool fwd_phase_fits(int H, int dtype);
 cudaError_t launch_fwd_phase(const FwdArgs &a, int dtype, int mode, int sm_count, cudaStream_t st);
+// The same rows of 4-32 KB (plain, residual-fused, LayerNorm): the bulk-copy
+// ring, each row's frame staged whole.
+bool plan_fwd_ring_phase(int64_t M, int H, int dtype, int mode, int sm_count, RingPlan *out);
+cudaError_t launch_fwd_ring_phase(const FwdArgs &a, int dtype, int mode, const RingPlan &p, cudaStream_t st);
 
 // Aligned rows above 32 KB: a cluster of CTAs per row, one segment each.
 bool plan_fwd_split(int64_t M, int H, int dtype, int mode, int sm_count, SplitPlan *out);
@@ -105,7 +109,7 @@ cudaError_t launch_fwd_chunked(const FwdArgs &a, int dtype, int mode, bool vec, 
 
 // Backward: dx per row plus per-CTA dweight partials, then the fixed-order
 // column reduction of the partials.
-enum BwdKind { kBwdRow = 0, kBwdChunked = 1, kBwdRing = 2, kBwdSplit = 3, kBwdPhase = 4 };
+enum BwdKind { kBwdRow = 0, kBwdChunked = 1, kBwdRing = 2, kBwdSplit = 3, kBwdPhase = 4, kBwdRingPhase = 5 };
 struct BwdPlan {
     int kind;          // BwdKind
     bool dres;         // adds the residual stream's gradient (fused-forward backward)
@@ -124,6 +128,9 @@ const void *bwd_split_kernel_for(int dtype, int nv, bool dres);
 // alignment phase: the register-row backward in each row's aligned frame.
 bool bwd_phase_pick(int H, int dtype, int *threads, int *nv);
 const void *bwd_phase_kernel_for(int dtype, int nv, bool dres);
+// The same rows of 2-32 KB: the bulk-copy ring, each row's frame staged whole.
+bool bwd_ring_phase_geometry(int H, int dtype, bool dres, RingPlan *p);
+const void *bwd_ring_phase_kernel_for(int dtype, int nv, bool dres);
 // `phased`: the rows are not 16-byte aligned but share one phase (above).
 BwdPlan plan_bwd(int64_t M, int H, int dtype, bool vec, bool phased, bool dres, int sm_count);
 size_t bwd_partial_bytes(const BwdPlan &p, int H);

@@ -33,6 +33,17 @@ def test_long_rows_workload_is_registered_with_its_configuration():
     assert wl.CONFIGS[4]["name"] == "fwd_bwd_bf16_16384x8192"
 
 
+def test_odd_rows_workload_is_registered_with_its_configuration():
+    """The misaligned-row workload is selectable; its contiguous rows of an odd
+    length start at every element offset within 16 bytes in turn."""
+    import workloads as wl
+    assert "odd_rows" in bench.WORKLOADS
+    c = wl.CONFIGS[7]
+    assert c["H"] % 2 == 1 and c["stride"] == c["H"] and c["dtype"] == "bf16"
+    offsets = {(r * c["stride"] * 2) % 16 for r in range(8)}
+    assert offsets == set(range(0, 16, 2))
+
+
 def test_aggregate_uses_slowest_rank():
     a = bench.aggregate([2.0, 4.0], units_per_rank=100, bytes_per_unit_rank=1e9)
     assert a["ms"] == 4.0

@@ -1,4 +1,4 @@
-"""GPU parity on the five named workloads (and the long-row case) at full size, through the same
+"""GPU parity on the five named workloads (and the long-row and odd-row cases) at full size, through the same
 binding calls the benchmark times.  The oracle checks every row element by element (in blocks of
 rows, to bound host memory): y within the forward tolerance, residual_out bit-exact, rrms within
 1e-5, dx within the backward tolerance, and the full dweight (an fp64 sum over every row); plus
@@ -156,4 +156,26 @@ def test_long_rows_fused_fwd_bwd_bf16(oracle):
     rn.rmsnorm_bwd(gdy.t, gs.t, wd, rrms, gdx.t, dw, ws)
     torch.cuda.synchronize()
     fwd_check(oracle, cfg, d["x"], d["residual"], d["w"], gy, gs, rrms)
+    bwd_check(oracle, cfg, d["dy"], gs.host(), d["w"], gdx, dw)
+
+
+def test_odd_rows_fused_fwd_bwd_bf16(oracle):
+    """The misaligned-row measurement case (bf16 16384 x 4095, rows contiguous,
+    so they start at every element offset within 16 bytes: the aligned-frame
+    kernels) at full size, as the benchmark's odd_rows step runs it."""
+    cfg = wl.CONFIGS[7]
+    d = wl.generate(7)
+    M, H, S, dt = cfg["M"], cfg["H"], cfg["stride"], cfg["dtype"]
+    gx, gr = Guarded(M, H, S, dt).upload(d["x"]), Guarded(M, H, S, dt).upload(d["residual"])
+    gy, gs = Guarded(M, H, S, dt), Guarded(M, H, S, dt)
+    wd = device_vec(d["w"], dt)
+    rrms = f32_buffer(M)
+    rn.rmsnorm_fwd_residual(gx.t, gr.t, wd, gy.t, gs.t, rrms, eps=cfg["eps"])
+    gdy, gdx = Guarded(M, H, S, dt).upload(d["dy"]), Guarded(M, H, S, dt)
+    dw = f32_buffer(H)
+    ws = torch.empty(rn.rmsnorm_bwd_workspace_bytes(M, H, wl.torch_dtype(dt)), dtype=torch.uint8, device="cuda")
+    rn.rmsnorm_bwd(gdy.t, gs.t, wd, rrms, gdx.t, dw, ws)
+    torch.cuda.synchronize()
+    fwd_check(oracle, cfg, d["x"], d["residual"], d["w"], gy, gs, rrms)
+    assert gx.untouched_outside() and gr.untouched_outside()
     bwd_check(oracle, cfg, d["dy"], gs.host(), d["w"], gdx, dw)

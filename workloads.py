@@ -146,6 +146,11 @@ CONFIGS = {
     # a measurement case beside the five configurations above
     6: dict(name="fused_fwd_bwd_bf16_4096x32768", dtype="bf16", M=4096, H=32768, stride=32768, eps=1e-5,
             seed=5, residual=True, weight=True, backward=True, save_rrms=True),
+    # rows that are not 16-byte aligned: an odd hidden size, rows contiguous,
+    # so a row starts at each of the 8 element offsets within 16 bytes in turn
+    # (the aligned-frame kernels); a measurement case beside the five above
+    7: dict(name="fused_fwd_bwd_bf16_16384x4095", dtype="bf16", M=16384, H=4095, stride=4095, eps=1e-5,
+            seed=6, residual=True, weight=True, backward=True, save_rrms=True),
 }
 
 
