@@ -280,6 +280,18 @@ bool plan_fwd_ring_phase(int64_t M, int H, int dtype, int mode, int sm_count, Ri
     if (p.smem_bytes > 200 * 1024) return false;
     const void *k = kernel_for(dtype, mode, p.nv);
     if (k == nullptr || allow_dynamic_smem(k, p.smem_bytes) != cudaSuccess) return false;
+    // one CTA per SM (fused rows from 12 KB): two of two stages instead, so
+    // while slot 0's thread finishes the row's two partial vectors and holds
+    // its CTA at the barrier, the other CTA's rows stream
+    if (p.max_ctas_per_sm == 1) {
+        const int streams = (mode == kResid || mode == kLnResid) ? 2 : 1;
+        const size_t smem = kRingHeaderBytes + (size_t)2 * streams * p.shape.row_pitch;
+        if (allow_dynamic_smem(k, smem) == cudaSuccess && occupancy(k, p.threads, smem) >= 2) {
+            p.shape.stages = 2;
+            p.smem_bytes = smem;
+            p.max_ctas_per_sm = 2;
+        }
+    }
     int occ = occupancy(k, p.threads, p.smem_bytes);
     if (occ <= 0) return false;
     if (p.max_ctas_per_sm > 0 && occ > p.max_ctas_per_sm) occ = p.max_ctas_per_sm;
