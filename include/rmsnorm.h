@@ -28,8 +28,15 @@
  *     and dx (rmsn_dtype).  Arithmetic is binary32; every stored result is
  *     rounded to nearest, ties to even.  rrms and dweight are binary32.
  *   - Every pointer must be aligned to its element size.  Rows whose byte
- *     offsets and lengths are multiples of 16 use 128-bit accesses; other
- *     layouts run a scalar-access variant of the same kernels (on the GPU).
+ *     offsets and lengths are multiples of 16 use 128-bit accesses.  Rows
+ *     that are not (an odd H, a stride or a view that is not a multiple of 16
+ *     bytes) still use 128-bit accesses, in each row's own 16-byte-aligned
+ *     frame with its first and last vectors masked, when the row matrices of
+ *     the call (x, residual, y, residual_out; dy, x, dx, dresidual_out)
+ *     start at the same offset modulo 16 bytes; those kernels read (never
+ *     write) the bytes that share a 16-byte granule with a row's first or
+ *     last element.  Other layouts run a scalar-access variant of the same
+ *     kernels (on the GPU).
  *   - stream is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     only enqueue work and return; errors raised while the kernels run
  *     surface at the caller's next synchronisation.
@@ -267,7 +274,8 @@ int rmsnorm_read_device_errors(unsigned *flags);
  *     the bulk-copy ring kernels (16-byte aligned rows of 4-32 KB for the
  *     plain, LayerNorm and shared-conditioning AdaLN forwards, 8-32 KB for
  *     the residual-fused and per-token AdaLN forwards, 2-32 KB for the
- *     backwards) wait for its first row before it has issued any copy, so
+ *     backwards, and their aligned-frame variants for rows that are not
+ *     16-byte aligned) wait for its first row before it has issued any copy, so
  *     that wait runs out on purpose and sets RMSN_DEVERR_PIPELINE_TIMEOUT;
  *     the kernel then issues its copies and finishes.
  * Outputs of calls made under these settings are unreliable.  The settings
